@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 INT4-weight MoE layer (sigmoid+bias routing) on GB300.
+
+A step is one pass of the whole layer over one batch: route, align, gate/up
+GEMM with fused SiLU*mul, down GEMM, top-k weighted sum.  Default workload:
+the Kimi-K2 EP8 decode shard (64 tokens, hidden 7168, intermediate 2048, 48
+of 384 experts local, top-8).  Inputs are seeded synthetic data of that shape;
+weights are random INT4 with BF16 group-32 scales.
+
+Timing: L2 is never warm across steps: the loop rotates over R independent
+layer replicas (distinct weights and inputs, like consecutive layers of a
+model), and every step's own weight working set already exceeds the 129 MB
+L2.  Steps run as four CUDA-graph replays (route+align, gate/up, down,
+combine) with CUDA events between them, so each kernel's duration is taken
+live inside the timed region; the whole region is bracketed by a barrier and
+torch.cuda.synchronize(), and the max over ranks is reported.
+
+`e2e` repeats the measurement through the public single call
+(chord_moe_layer) with pinned HOST inputs and outputs: each step copies x
+and the router logits host->device and the layer output device->host.
+
+`--impl reference` times the CPU oracle (numpy, FP64) on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A16 MoE layer tokens/s; decode HBM GB/s, prefill TFLOPS vs GB300 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+KERNEL_SOURCES = {
+    "gate_up": ["w4a16_int4_weight_sigmoid_gb300/csrc/gemm_small.cu",
+                "w4a16_int4_weight_sigmoid_gb300/csrc/common.cuh"],
+    "down": ["w4a16_int4_weight_sigmoid_gb300/csrc/gemm_small.cu",
+             "w4a16_int4_weight_sigmoid_gb300/csrc/common.cuh"],
+}
+
+
+def parse_args():
+    from w4a16_int4_weight_sigmoid_gb300 import workload as wl
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(wl.WORKLOADS), default=wl.EP8_DECODE.name)
+    p.add_argument("--replicas", type=int, default=4)
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--cpu-budget-s", type=float, default=20.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    sources are unchanged since the capture; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        entries = json.load(f)
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload:
+            if e.get("source_sha") == source_sha(KERNEL_SOURCES[kernel]):
+                return e.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.out = ""
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.out, _ = self.proc.communicate()
+        return self.summary()
+
+    def summary(self):
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# --------------------------------------------------------------- workloads
+class Replica:
+    """One layer's weights, inputs and buffers on the device."""
+
+    def __init__(self, shape, seed, device, keep_host=False):
+        import torch
+        from w4a16_int4_weight_sigmoid_gb300 import chord
+        from w4a16_int4_weight_sigmoid_gb300 import workload as wl
+        from w4a16_int4_weight_sigmoid_gb300.layer import W4A16MoELayer, to_device
+        self.shape = shape
+        d = wl.layer_inputs(shape, seed)
+        self.host = d if keep_host else None
+        self.layer = W4A16MoELayer(d["w13_q"], d["w13_s"], d["w2_q"], d["w2_s"], shape.E_total,
+                                   shape.expert_begin, shape.topk, device=device)
+        self.x = to_device(d["x"], device)
+        self.logits = to_device(d["logits"], device)
+        self.bias = to_device(d["bias"], device)
+        self.x_pinned = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        self.logits_pinned = torch.from_numpy(d["logits"]).pin_memory()
+        del d
+        M, k, E, H, I = shape.M, shape.topk, shape.E_local, shape.H, shape.I
+        self.bm = 16
+        self.cap = chord.chord_moe_align_capacity(M, k, E, self.bm)
+        i32, dev = torch.int32, device
+        self.tw = torch.empty((M, k), dtype=torch.float32, device=dev)
+        self.ti = torch.empty((M, k), dtype=torch.int32, device=dev)
+        self.sorted = torch.empty(self.cap, dtype=i32, device=dev)
+        self.eids = torch.empty(self.cap // self.bm, dtype=i32, device=dev)
+        self.ntpp = torch.empty(1, dtype=i32, device=dev)
+        self.counts = torch.empty(E, dtype=i32, device=dev)
+        self.offsets = torch.empty(E + 1, dtype=i32, device=dev)
+        self.pos = torch.empty(M * k, dtype=i32, device=dev)
+        wsb = chord.chord_moe_align_workspace_bytes(M, k, E)
+        self.aws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
+        self.h = torch.empty((self.cap, I), dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty((self.cap, H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=i32, device=dev)
+        self.plan = chord.chord_moe_layer_plan(M, shape.E_total, k)
+        self.align_launches = 1 if wsb == 0 else 2
+
+    # the layer's steps, each one C-ABI call (the calls chord_moe_layer makes)
+    def route_align(self):
+        from w4a16_int4_weight_sigmoid_gb300 import chord
+        s = self.shape
+        chord.chord_moe_route(self.logits, self.bias, s.topk, self.tw, self.ti)
+        chord.chord_moe_align(self.ti, s.expert_begin, s.E_local, self.bm, self.sorted, self.eids,
+                              self.ntpp, self.counts, self.offsets, self.pos, self.aws)
+
+    def gate_up(self):
+        from w4a16_int4_weight_sigmoid_gb300 import chord
+        s = self.shape
+        chord.chord_w4a16_moe_gemm(self.x, True, self.layer.w13, s.E_local, 2 * s.I, s.H, s.M, s.topk,
+                                   self.sorted, self.counts, self.offsets, chord.CHORD_EPI_SILU_MUL,
+                                   self.h, tuning=self.plan, dev_status=self.status)
+
+    def down(self):
+        from w4a16_int4_weight_sigmoid_gb300 import chord
+        s = self.shape
+        chord.chord_w4a16_moe_gemm(self.h, False, self.layer.w2, s.E_local, s.H, s.I, s.M, s.topk,
+                                   self.sorted, self.counts, self.offsets, chord.CHORD_EPI_STORE,
+                                   self.y, tuning=self.plan, dev_status=self.status)
+
+    def combine(self):
+        from w4a16_int4_weight_sigmoid_gb300 import chord
+        chord.chord_moe_sum(self.y, self.tw, self.pos, self.out)
+
+    def capture(self):
+        import torch
+        self.graphs = []
+        for fn in (self.route_align, self.gate_up, self.down, self.combine):
+            fn()                      # eager run first: sets kernel attributes
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def stats(self):
+        """Touched experts and local rows of this replica's routing."""
+        c = self.counts.cpu().numpy()
+        return int((c > 0).sum()), int(c.sum())
+
+
+def algorithmic(shape, touched, rows):
+    """Bytes and FLOPs one launch of each GEMM must move / do (padding rows
+    not counted): touched experts' INT4 weights + BF16 scales, activation rows
+    in, rows out."""
+    H, I = shape.H, shape.I
+    w13 = 2 * I * H // 2 + 2 * I * (H // 32) * 2
+    w2 = H * I // 2 + H * (I // 32) * 2
+    return {
+        "gate_up": {"bytes": touched * w13 + rows * H * 2 + rows * I * 2, "flops": 2 * rows * 2 * I * H},
+        "down": {"bytes": touched * w2 + rows * I * 2 + rows * H * 2, "flops": 2 * rows * H * I},
+    }
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+    from w4a16_int4_weight_sigmoid_gb300 import build as B
+    from w4a16_int4_weight_sigmoid_gb300 import chord
+    from w4a16_int4_weight_sigmoid_gb300 import workload as wl
+
+    B.build()
+    chord.lib()
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    shape = wl.WORKLOADS[args.workload]
+    decode = shape.M * shape.topk / shape.E_total < 64
+    steps = args.steps if args.steps is not None else (20000 if decode else 300)
+    warmup = max(3, args.warmup if args.warmup is not None else (200 if decode else 10))
+    R = max(1, args.replicas)
+    reps = [Replica(shape, shape.seed + 1000 * r + 7919 * rank, device, keep_host=(r == 0))
+            for r in range(R)]
+    for r in reps:
+        r.capture()
+
+    # warm-up
+    for i in range(warmup):
+        for g in reps[i % R].graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    for r in reps:
+        assert r.status.item() == 0, f"device status {r.status.item()}"
+    st = [r.stats() for r in reps]
+
+    nev = 5
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        if uuid and not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t0.record()
+    for i in range(steps):
+        e = evs[i]
+        gs = reps[i % R].graphs
+        e[0].record()
+        gs[0].replay()
+        e[1].record()
+        gs[1].replay()
+        e[2].record()
+        gs[2].replay()
+        e[3].record()
+        gs[3].replay()
+        e[4].record()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed_ms = allreduce_max(t0.elapsed_time(t1), world)
+    names = ["route_align", "gate_up", "down", "combine"]
+    per = {n: [] for n in names}
+    for e in evs:
+        for j, n in enumerate(names):
+            per[n].append(e[j].elapsed_time(e[j + 1]))
+    kern_us = {n: 1000.0 * statistics.fmean(v) for n, v in per.items()}
+
+    # algorithmic work per launch, averaged over the replica rotation
+    alg = {"gate_up": {"bytes": 0.0, "flops": 0.0}, "down": {"bytes": 0.0, "flops": 0.0}}
+    for i in range(steps):
+        a = algorithmic(shape, *st[i % R])
+        for k in alg:
+            for q in ("bytes", "flops"):
+                alg[k][q] += a[k][q] / steps
+
+    peaks, peak_src = load_peaks()
+    dom = max(("gate_up", "down"), key=lambda n: kern_us[n])
+    t_s = kern_us[dom] * 1e-6
+    t_hbm = alg[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg[dom]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12)
+    if t_hbm >= t_tc:
+        ach = alg[dom]["bytes"] / t_s / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        ach = alg[dom]["flops"] / t_s / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = committed_traffic(dom, shape.name)
+    roof["kernel"] = f"gemm_small ({dom})"
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["algorithmic_bytes_per_launch"] = alg[dom]["bytes"]
+    roof["algorithmic_flops_per_launch"] = alg[dom]["flops"]
+
+    # whole-layer roofline: slower of bytes at HBM peak and FLOPs at BF16 peak
+    lay_bytes = alg["gate_up"]["bytes"] + alg["down"]["bytes"]
+    lay_flops = alg["gate_up"]["flops"] + alg["down"]["flops"]
+    t_lay_min = max(lay_bytes / (peaks["hbm_gbs"] * 1e9), lay_flops / (peaks["bf16_tflops_sustained"] * 1e12))
+    ms_per_step = elapsed_ms / steps
+    value = shape.M * steps * world / (elapsed_ms / 1e3)
+
+    # ----------------------------------------------------------- e2e
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, steps // 10)
+    outs_pinned = [torch.empty((shape.M, shape.H), dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+    for i in range(3):
+        r = reps[i % R]
+        r.layer.forward(r.x, r.logits, r.bias, out=r.out)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e2e_steps):
+        r = reps[i % R]
+        r.x.copy_(r.x_pinned, non_blocking=True)
+        r.logits.copy_(r.logits_pinned, non_blocking=True)
+        r.layer.forward(r.x, r.logits, r.bias, out=r.out)
+        outs_pinned[i % R].copy_(r.out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = allreduce_max(e0.elapsed_time(e1), world)
+    h2d = shape.M * shape.H * 2 + shape.M * shape.E_total * 4
+    d2h = shape.M * shape.H * 2
+    e2e = {"value": shape.M * e2e_steps * world / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "api": "chord_moe_layer"}
+
+    launches_per_step = reps[0].align_launches + 4
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": shape.name, "M": shape.M, "H": shape.H, "I": shape.I,
+                   "E_total": shape.E_total, "E_local": shape.E_local, "topk": shape.topk,
+                   "weights": "INT4 group-32 symmetric, BF16 scales; BF16 activations",
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {R} rotating layer replicas, each step's touched "
+                         f"weights ~{alg['gate_up']['bytes'] / 1e6 + alg['down']['bytes'] / 1e6:.0f} MB "
+                         f"> 129 MB L2",
+                   "touched_experts_per_replica": [s[0] for s in st],
+                   "local_rows_per_replica": [s[1] for s in st]},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * steps,
+        "roofline": roof,
+        "layer_roofline": {"bytes": lay_bytes, "flops": lay_flops, "t_min_us": t_lay_min * 1e6,
+                           "t_us": ms_per_step * 1e3, "frac": t_lay_min / (ms_per_step * 1e-3)},
+        "kernels_us": kern_us,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, reps[0].host, args.cpu_budget_s)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------- oracle timing
+def oracle_tokens_per_s(shape, host, budget_s, max_tokens=None):
+    """Time the oracle on a bounded sample of tokens that have local experts."""
+    import oracle
+    w, ids, _ = oracle.route(host["logits"], host["bias"], shape.topk)
+    local = np.any((ids >= shape.expert_begin) & (ids < shape.expert_begin + shape.E_local), axis=1)
+    cand = np.nonzero(local)[0]
+    n, t_total, done = 0, 0.0, []
+    for tok in cand:
+        t = time.perf_counter()
+        oracle.moe_layer_tokens(np.array([tok]), host["x"], host["logits"], host["bias"], host["w13_q"],
+                                host["w13_s"], host["w2_q"], host["w2_s"], shape.topk, shape.expert_begin)
+        t_total += time.perf_counter() - t
+        n += 1
+        done.append(int(tok))
+        if t_total >= budget_s or (max_tokens and n >= max_tokens):
+            break
+    return n / t_total, n, t_total
+
+
+def cpu_baseline(shape, host, budget_s):
+    v, n, t = oracle_tokens_per_s(shape, host, budget_s)
+    return {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} tokens (each with >= 1 local expert) of {shape.name}, one at a time "
+                      f"through the FP64 numpy oracle, {t:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from w4a16_int4_weight_sigmoid_gb300 import workload as wl
+    shape = wl.WORKLOADS[args.workload]
+    host = wl.layer_inputs(shape)
+    steps = args.steps if args.steps is not None else 8
+    warmup = args.warmup if args.warmup is not None else 1
+    # each step is one token; stop early when the time budget runs out
+    budget = 150.0
+    oracle_tokens_per_s(shape, host, 1e9, max_tokens=max(1, min(warmup, 2)))
+    v, n, t = oracle_tokens_per_s(shape, host, budget, max_tokens=steps)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": n, "warmup": warmup, "ms_per_step": 1e3 * t / n, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": shape.name, "M": shape.M, "H": shape.H, "I": shape.I,
+                       "E_total": shape.E_total, "E_local": shape.E_local, "topk": shape.topk},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{n} tokens of {shape.name} (one per step), FP64 numpy oracle"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,217 @@
+/*
+ * chord_moe.h -- C ABI of the GB300 (sm_103a) W4A16 INT4-weight MoE layer.
+ *
+ * The layer: sigmoid+bias top-k routing -> moe_align_block_size -> grouped
+ * gate/up GEMM (INT4 group-32 weights, BF16 scales, BF16 activations,
+ * dequantised in-kernel) with fused SiLU*mul -> grouped down GEMM -> top-k
+ * weighted sum back to tokens.
+ *
+ * Sources, cited by page title and section:
+ *   [Chord]   "vLLM 및 Novita AI, Kimi K2.x용 더 빠른 INT4 MoE 커널 출시: Chord"
+ *   [HumPR]   "[vllm] vLLM에 고성능 JIT 양자화 커널 'Humming' 도입하기"
+ *   [Router]  "[flashinfer] FlashInfer, B200 GPU에서 Kimi-K3 MoE 라우터 성능 최적화"
+ *   [Humming] "Humming: vLLM과 Ant Group, 양자화 추론을 위한 범용 커널 라이브러리
+ *              오픈소스 공개"
+ *
+ * Conventions for every entry point:
+ *   - Pointers named in the signature are DEVICE pointers unless a comment
+ *     says otherwise; the caller owns all memory.  No entry point allocates
+ *     device memory or synchronises the stream; `stream` is a cudaStream_t
+ *     passed as void* (NULL = legacy default stream).
+ *   - BF16 tensors are passed as chord_bf16 (the raw 16-bit pattern).
+ *   - Tensors are dense, row-major, and 16-byte aligned.
+ *   - Return value: CHORD_OK or a negative CHORD_ERR_* code from host-side
+ *     checks or the launch; nothing is launched when a check fails.
+ *     chord_last_error_string() describes the last failure on this thread.
+ *   - Errors found on the device (packed-weight header mismatch, a bounded
+ *     wait that ran out, invalid routing) are written with an atomic
+ *     compare-and-swap into the caller's `dev_status` int (first error wins;
+ *     the caller zeroes it and reads it when convenient, which keeps every
+ *     call capturable in a CUDA graph: [Chord] "런타임 고려사항" notes graph
+ *     capture is possible when routing validation is off).
+ */
+#ifndef CHORD_MOE_H
+#define CHORD_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t chord_bf16;
+
+enum chord_status {
+  CHORD_OK = 0,
+  CHORD_ERR_INVALID_ARG = -1,       /* null pointer, bad shape, misalignment */
+  CHORD_ERR_UNSUPPORTED = -2,       /* a compute option this library does not implement */
+  CHORD_ERR_CUDA = -3,              /* a CUDA runtime call or launch failed */
+  CHORD_ERR_WORKSPACE_TOO_SMALL = -4,
+  CHORD_ERR_PREPACK_MISMATCH = -5,  /* packed-weight header does not match the call */
+  CHORD_ERR_TIMEOUT = -6,           /* a bounded device wait ran out (device status) */
+  CHORD_ERR_ROUTING_INVALID = -7    /* an expert id out of range (device status) */
+};
+
+/* GEMM epilogues. */
+enum chord_epilogue {
+  CHORD_EPI_STORE = 0,    /* C[r, n] = bf16(acc[r, n]) */
+  CHORD_EPI_SILU_MUL = 1  /* C[r, i] = bf16(silu(acc[r, i]) * acc[r, I + i]), I = N/2 */
+};
+
+/* GEMM execution paths. */
+enum chord_path {
+  CHORD_PATH_AUTO = 0,    /* choose from the expected tokens per expert */
+  CHORD_PATH_SMALL_M = 1, /* register-MMA weight-streaming path (decode) */
+  CHORD_PATH_LARGE_M = 2  /* tcgen05 / TMEM path (prefill) */
+};
+
+/* Optional tuning overrides; pass NULL for the built-in heuristics.  The two
+ * compute options mirror Humming's compute config ([HumPR] "코드 분석" 2,
+ * use_batch_invariant / use_f16_accum); like the backends on [Chord]
+ * "런타임 고려사항", this library does not implement them and returns
+ * CHORD_ERR_UNSUPPORTED when either is set. */
+typedef struct chord_tuning {
+  int path;             /* chord_path */
+  int rows_per_pass;    /* small-M path: token rows per weight pass, 8/16/32; 0 = heuristic */
+  int use_f16_accum;    /* must be 0 */
+  int batch_invariant;  /* must be 0 */
+} chord_tuning;
+
+/* Description of the last failure on the calling thread ("" if none). */
+const char* chord_last_error_string(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int chord_version(void);
+
+/* ---------------------------------------------------------------- routing
+ * Sigmoid + bias top-k router.  Buffers follow the fused router's argument
+ * plan ([Router] "코드 분석": logits, bias, topk_weights, topk_ids).
+ *   logits       FP32 [M, E_total]   router logits (finite values)
+ *   bias         FP32 [E_total]      expert score-correction bias
+ *   topk_weights FP32 [M, topk]      out: s_j / sum of the selected s
+ *   topk_ids     INT32 [M, topk]     out: selected experts, largest key first
+ * Per token: s_e = sigmoid(logit_e) in a fixed binary32 op sequence (range
+ * reduction n = rint(y*log2e), r = (y - n*ln2_hi) - n*ln2_lo with
+ * y = clamp(-x, -87, 87); degree-7 Taylor polynomial in Horner form with
+ * separately rounded multiply and add; times 2^n; s = 1/(1+e)), so results
+ * are bit-identical across implementations of the same sequence; key_e =
+ * s_e + bias_e; the topk largest keys win, equal keys going to the lower id.
+ * Requires 1 <= topk <= min(E_total, 32), 1 <= E_total <= 1024, M >= 0.
+ */
+int chord_moe_route(const float* logits, const float* bias, int M, int E_total, int topk,
+                    float* topk_weights, int32_t* topk_ids, void* stream);
+
+/* ------------------------------------------------------------------ align
+ * moe_align_block_size: group the M*topk assignments by local expert and pad
+ * each group to a multiple of block_m ([Router] "코드 분석" arg_plan:
+ * sorted_token_ids, expert_ids, num_tokens_post_padded, expert_counts,
+ * expert_offsets; [Chord] "런타임 고려사항": over-allocated buffers).
+ *   topk_ids          INT32 [M, topk]  expert of assignment f = t*topk + j
+ *   expert_begin, E_local              local experts [begin, begin+E_local);
+ *                                      other assignments are dropped
+ *   block_m           8, 16, 32, 64 or 128
+ *   capacity          rows of sorted_token_ids; must be >= chord_moe_align_capacity()
+ *   sorted_token_ids  INT32 [capacity] out: expert e's flat indices f in
+ *                     ascending order at rows expert_offsets[e] ..; padding
+ *                     rows hold the sentinel M*topk; rows past
+ *                     num_tokens_post_padded are not written
+ *   expert_ids        INT32 [capacity/block_m] out: local expert of each block
+ *   num_tokens_post_padded INT32 [1] out: total padded rows
+ *   expert_counts     INT32 [E_local]   out: assignments per local expert
+ *   expert_offsets    INT32 [E_local+1] out: exclusive prefix of padded counts
+ *   sorted_positions  INT32 [M*topk] out (may be NULL): row of assignment f,
+ *                     or -1 if its expert is not local
+ *   workspace         device scratch of chord_moe_align_workspace_bytes()
+ *                     bytes (may be NULL when that is 0)
+ * The per-expert cursors the page calls expert_scatter_offsets live in the
+ * workspace and are re-initialised by every call.
+ */
+size_t chord_moe_align_capacity(int M, int topk, int E_local, int block_m);
+size_t chord_moe_align_workspace_bytes(int M, int topk, int E_local);
+int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, int E_local,
+                    int block_m, size_t capacity, int32_t* sorted_token_ids, int32_t* expert_ids,
+                    int32_t* num_tokens_post_padded, int32_t* expert_counts,
+                    int32_t* expert_offsets, int32_t* sorted_positions, void* workspace,
+                    size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- prepack
+ * Repack INT4 weights and scales into this library's kernel layout
+ * ([Humming] "워크로드별 튜닝 및 JIT 컴파일": preprocessing validates
+ * parameters, pads dimensions and repacks into the target kernel's layout;
+ * [HumPR] "왜 이게 좋은가" 2: automatic padding of shape_n).
+ *   qweight  uint8 [E, N, K/2]  two's-complement nibbles, low nibble = even k
+ *   scales   BF16  [E, N, K/32] W[e,n,k] = q[e,n,k] * scales[e,n,k/32]
+ *   group    must be 32
+ *   gate_up  1: rows 0..N/2-1 are the gate projection and N/2..N-1 the up
+ *            projection (required for CHORD_EPI_SILU_MUL); 0 otherwise
+ *   packed   out, chord_w4a16_prepack_bytes() bytes, 16-byte aligned
+ * Requires K % 64 == 0; N % 16 == 0 (gate_up: N % 128 == 0).  N is padded
+ * to a multiple of 128 rows with zero weights.  The blob starts with a
+ * 256-byte header (magic, version, shapes, flags) that every GEMM launch
+ * checks on the device.
+ */
+size_t chord_w4a16_prepack_bytes(int E, int N, int K, int group);
+int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E, int N, int K,
+                        int group, int gate_up, void* packed, size_t packed_bytes, void* stream);
+
+/* ------------------------------------------------------- grouped W4A16 GEMM
+ * Indexed MoE GEMM ([Chord] "핵심 기여", "인덱스 커널 기법"): for every
+ * local expert e and row r in expert_offsets[e] .. + expert_counts[e]:
+ *   acc[r, n] = sum_k A[row(r), k] * q[e, n, k] * s[e, n, k/32]   (FP32 accumulate)
+ * with row(r) = sorted_token_ids[r] / topk when a_gather = 1 (A = the
+ * token activations [M, K]) and row(r) = r when a_gather = 0 (A = rows in
+ * sorted order [capacity, K], e.g. the gate/up output).
+ *   C        BF16 [capacity, N] (STORE) or [capacity, N/2] (SILU_MUL); padding
+ *            rows are not written
+ *   dev_status  device int for errors found on the device (may be NULL)
+ * The expert offsets/counts are read on the device, so the call never waits
+ * for the host (graph-safe).
+ */
+int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w, int E_local,
+                         int N, int K, int M, int topk, const int32_t* sorted_token_ids,
+                         const int32_t* expert_counts, const int32_t* expert_offsets,
+                         size_t capacity, int epilogue, chord_bf16* C, const chord_tuning* tuning,
+                         int* dev_status, void* stream);
+
+/* --------------------------------------------------------- top-k weighted sum
+ * moe_fused_mul_sum ([HumPR] "왜 이게 좋은가" 3: weight multiply and sum):
+ *   out[t, :] = sum over j = 0..topk-1 with sorted_positions[t*topk+j] >= 0 of
+ *               topk_weights[t, j] * y[sorted_positions[t*topk+j], :]
+ * accumulated in FP32 in increasing j, rounded once to BF16.  A token with
+ * no local assignment gets zeros.  Requires H % 8 == 0.
+ */
+int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions,
+                  int M, int topk, int H, chord_bf16* out, void* stream);
+
+/* ------------------------------------------------------------- whole layer
+ * One MoE layer on this GPU's expert shard: route, align, gate/up GEMM with
+ * fused SiLU*mul, down GEMM, top-k weighted sum ([Chord] "핵심 기여").
+ *   x            BF16 [M, H]
+ *   logits, bias as chord_moe_route (E_total experts)
+ *   w13_packed   prepacked gate|up weights [E_local, 2I, H] (gate_up = 1)
+ *   w2_packed    prepacked down weights [E_local, H, I]
+ *   out          BF16 [M, H]
+ *   topk_weights_out FP32 [M, topk], topk_ids_out INT32 [M, topk]: optional
+ *                copies of the routing (may be NULL)
+ *   workspace    chord_moe_layer_workspace_bytes() bytes
+ * The expert-parallel shard is implied by E_local < E_total ([Chord]
+ * "런타임 고려사항": the profile is inferred from the shapes, no shard
+ * argument).  Weights are normalised over all topk experts, local or not.
+ */
+size_t chord_moe_layer_workspace_bytes(int M, int H, int I, int E_local, int topk);
+/* Host-only: the tuning chord_moe_layer uses for these shapes (tokens-per-
+ * expert policy, [Chord] "인덱스 커널 기법": the schedule follows the tokens
+ * delivered per expert, tok_e = M*topk/E_total).  Writes *plan; returns
+ * CHORD_OK or CHORD_ERR_INVALID_ARG.  Passing the plan to
+ * chord_w4a16_moe_gemm reproduces the layer's launches exactly. */
+int chord_moe_layer_plan(int M, int E_total, int topk, chord_tuning* plan);
+int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
+                    const void* w13_packed, const void* w2_packed, int M, int H, int I,
+                    int E_total, int expert_begin, int E_local, int topk, chord_bf16* out,
+                    float* topk_weights_out, int32_t* topk_ids_out, void* workspace,
+                    size_t ws_bytes, const chord_tuning* tuning, int* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CHORD_MOE_H */

@@ -1,0 +1,132 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+entry point include/chord_moe.h declares; host-side sizing functions; argument
+checks that reject bad calls before any launch; the header is plain C."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from w4a16_int4_weight_sigmoid_gb300 import build as B
+from w4a16_int4_weight_sigmoid_gb300 import chord
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "chord_moe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return chord.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(chord_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (chord_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_binding_covers_every_entry_point():
+    assert set(_declared()) == set(chord._SIGS)
+
+
+def test_header_is_plain_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "chord_moe.h"\nint main(void){return CHORD_OK;}\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), "-c",
+                        str(src), "-o", str(tmp_path / "t.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_sizing_functions(L):
+    assert L.chord_moe_align_capacity(3, 2, 4, 8) == 40             # 6 + 4*7 = 34 -> 40
+    assert L.chord_moe_align_capacity(4, 2, 8, 16) == 8 * 16
+    assert L.chord_moe_align_capacity(64, 8, 48, 16) == 512 + 48 * 15
+    assert L.chord_moe_align_capacity(1, 8, 384, 7) == 0           # bad block_m
+    assert L.chord_moe_align_workspace_bytes(128, 8, 384) == 0      # one chunk: none
+    assert L.chord_moe_align_workspace_bytes(4096, 8, 384) == (32768 + 8 * 384) * 4
+    assert L.chord_w4a16_prepack_bytes(48, 4096, 7168, 32) == 256 + 48 * 32 * 112 * 4608
+    assert L.chord_w4a16_prepack_bytes(1, 16, 64, 32) == 256 + 4608
+    assert L.chord_w4a16_prepack_bytes(1, 16, 96, 32) == 0          # K % 64
+    assert L.chord_w4a16_prepack_bytes(1, 16, 64, 64) == 0          # group 64
+    assert L.chord_moe_layer_workspace_bytes(64, 7168, 2048, 48, 8) > 0
+    assert L.chord_version() >= 100
+    plan = chord.chord_moe_layer_plan(64, 384, 8)
+    assert plan.path == chord.CHORD_PATH_SMALL_M and plan.rows_per_pass == 8
+    assert chord.chord_moe_layer_plan(128, 4, 2).rows_per_pass == 32
+
+
+def _rc_and_msg(L, rc):
+    return rc, L.chord_last_error_string().decode()
+
+
+def test_argument_checks_reject_before_launch(L):
+    P = ctypes.c_void_p(16)   # never dereferenced: the checks fail first
+    rc, msg = _rc_and_msg(L, L.chord_moe_route(P, P, 4, 384, 0, P, P, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "topk" in msg
+    rc, _ = _rc_and_msg(L, L.chord_moe_route(P, P, 4, 384, 33, P, P, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG
+    rc, _ = _rc_and_msg(L, L.chord_moe_route(P, P, 4, 2000, 8, P, P, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG
+    rc, msg = _rc_and_msg(L, L.chord_moe_align(P, 4, 2, 0, 8, 12, 1000, P, P, P, P, P, None, None, 0, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "block_m" in msg
+    rc, msg = _rc_and_msg(L, L.chord_moe_align(P, 4, 2, 0, 8, 16, 10, P, P, P, P, P, None, None, 0, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "capacity" in msg
+    rc, _ = _rc_and_msg(L, L.chord_moe_align(P, 4096, 8, 0, 384, 16, 10 ** 6, P, P, P, P, P, None, None, 0, None))
+    assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_prepack(P, P, 2, 128, 96, 32, 0, P, 10 ** 9, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_prepack(P, P, 2, 128, 128, 128, 0, P, 10 ** 9, None))
+    assert rc == chord.CHORD_ERR_UNSUPPORTED
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_prepack(P, P, 2, 96, 128, 32, 1, P, 10 ** 9, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG                        # gate_up needs N % 128
+    t = chord.chord_tuning(0, 0, 1, 0)
+    rc, msg = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, 100, 0, P,
+                                                    ctypes.byref(t), None, None))
+    assert rc == chord.CHORD_ERR_UNSUPPORTED and "FP16" in msg
+    t = chord.chord_tuning(0, 0, 0, 1)
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, 100, 0, P,
+                                                  ctypes.byref(t), None, None))
+    assert rc == chord.CHORD_ERR_UNSUPPORTED
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 100, 8, 2, P, P, P, 100, 0, P,
+                                                  None, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG                        # K % 64
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 192, 128, 8, 2, P, P, P, 100, 1, P,
+                                                  None, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG                        # SiLU needs N % 128
+    rc, _ = _rc_and_msg(L, L.chord_moe_sum(P, P, P, 4, 2, 100, P, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG                        # H % 8
+    rc, _ = _rc_and_msg(L, L.chord_moe_layer(P, P, P, P, P, 4, 256, 128, 8, 4, 8, 2, P, None, None,
+                                             P, 10 ** 9, None, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG                        # shard exceeds E_total
+    rc, _ = _rc_and_msg(L, L.chord_moe_layer(P, P, P, P, P, 4, 256, 128, 8, 0, 8, 2, P, None, None,
+                                             P, 10, None, None, None))
+    assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(chord, "_lib", None)
+    monkeypatch.setattr(chord, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        chord.lib()
+
+
+def test_product_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "w4a16_int4_weight_sigmoid_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "oracle/" not in text, f

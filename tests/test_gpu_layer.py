@@ -1,0 +1,87 @@
+"""GPU parity: the whole layer (chord_moe_layer) against the FP64 oracle.
+
+Small shapes are compared on every output element; the Kimi-K2 workloads are
+run at full size in the same call the benchmark times, and compared on a
+seeded sample of tokens that the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from w4a16_int4_weight_sigmoid_gb300 import workload as wl
+from w4a16_int4_weight_sigmoid_gb300.layer import W4A16MoELayer
+
+from gpu_util import assert_close_to_oracle, bf16_to_np, ensure_lib, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def run_layer(shape, d, **kw):
+    layer = W4A16MoELayer(d["w13_q"], d["w13_s"], d["w2_q"], d["w2_s"], shape.E_total,
+                          shape.expert_begin, shape.topk)
+    M = shape.M
+    tw = torch.empty((M, shape.topk), dtype=torch.float32, device="cuda")
+    ti = torch.empty((M, shape.topk), dtype=torch.int32, device="cuda")
+    out = layer.forward(to_device(d["x"]), to_device(d["logits"]), to_device(d["bias"]),
+                        topk_weights_out=tw, topk_ids_out=ti, **kw)
+    torch.cuda.synchronize()
+    assert layer.dev_status.item() == 0
+    return layer, bf16_to_np(out), tw.cpu().numpy(), ti.cpu().numpy()
+
+
+def small(name, M, H, I, E_total, E_local, begin, topk, seed, zipf=0.0):
+    return wl.LayerShape(name, M, H, I, E_total, E_local, begin, topk, seed, zipf)
+
+
+SMALL = [
+    wl.TINY,
+    small("ep_shard_ragged", 40, 512, 256, 16, 6, 5, 4, 21),
+    small("tp_zipf", 48, 256, 192, 32, 32, 0, 6, 22, zipf=1.1),
+    small("single_token", 1, 384, 128, 12, 12, 0, 3, 23),
+    small("top1_one_expert", 9, 128, 64, 1, 1, 0, 1, 24),
+    small("many_rows_per_expert", 256, 256, 128, 4, 4, 0, 2, 25),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+def test_layer_small_full_parity(shape):
+    d = wl.layer_inputs(shape)
+    ref, w, ids = oracle.moe_layer(d["x"], d["logits"], d["bias"], d["w13_q"], d["w13_s"],
+                                   d["w2_q"], d["w2_s"], shape.topk, shape.expert_begin)
+    for _ in range(2):
+        _, got, gw, gids = run_layer(shape, d)
+        assert np.array_equal(gids, ids)
+        assert np.array_equal(gw.view(np.uint32), w.view(np.uint32))
+        assert_close_to_oracle(got, ref, shape.name)
+
+
+def test_layer_tokens_without_local_experts_are_zero():
+    shape = small("shard_far", 24, 256, 128, 64, 4, 60, 2, 26)
+    d = wl.layer_inputs(shape)
+    _, got, _, gids = run_layer(shape, d)
+    none_local = ~np.any((gids >= 60) & (gids < 64), axis=1)
+    assert none_local.any()
+    assert np.all(got[none_local] == 0)
+
+
+@pytest.mark.parametrize("shape", [wl.EP8_DECODE, wl.TP8_DECODE, wl.EP8_PREFILL],
+                         ids=lambda s: s.name)
+def test_layer_kimi_workloads_sampled(shape):
+    d = wl.layer_inputs(shape)
+    _, got, gw, gids = run_layer(shape, d)
+    w, ids, _ = oracle.route(d["logits"], d["bias"], shape.topk)
+    assert np.array_equal(gids, ids)
+    assert np.array_equal(gw.view(np.uint32), w.view(np.uint32))
+    rng = np.random.default_rng(shape.seed)
+    local = np.any((ids >= shape.expert_begin) & (ids < shape.expert_begin + shape.E_local), axis=1)
+    cand = np.nonzero(local)[0]
+    tokens = np.sort(rng.choice(cand, size=min(6, cand.size), replace=False))
+    ref = oracle.moe_layer_tokens(tokens, d["x"], d["logits"], d["bias"], d["w13_q"], d["w13_s"],
+                                  d["w2_q"], d["w2_s"], shape.topk, shape.expert_begin)
+    assert_close_to_oracle(got[tokens], ref, shape.name)
+    assert np.all(np.isfinite(got))

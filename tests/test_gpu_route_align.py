@@ -1,0 +1,143 @@
+"""GPU parity: router and align kernels against the oracle, bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from w4a16_int4_weight_sigmoid_gb300 import chord
+from w4a16_int4_weight_sigmoid_gb300 import workload as wl
+
+from gpu_util import ensure_lib
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def gpu_route(logits, bias, k):
+    lg = torch.from_numpy(logits).cuda()
+    bs = torch.from_numpy(bias).cuda()
+    M = logits.shape[0]
+    w = torch.full((M, k), -1.0, dtype=torch.float32, device="cuda")
+    ids = torch.full((M, k), -1, dtype=torch.int32, device="cuda")
+    chord.chord_moe_route(lg, bs, k, w, ids)
+    torch.cuda.synchronize()
+    return w.cpu().numpy(), ids.cpu().numpy()
+
+
+def check_route(logits, bias, k):
+    w, ids, _ = oracle.route(logits, bias, k)
+    for _ in range(2):   # twice: catches nondeterminism
+        gw, gids = gpu_route(logits, bias, k)
+        assert np.array_equal(gids, ids)
+        assert np.array_equal(gw.view(np.uint32), w.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", wl.ROUTER_ALIGN_M)
+def test_route_router_workload(M):
+    logits, bias = wl.router_inputs(M, wl.ROUTER_ALIGN_E, wl.ROUTER_ALIGN_SEED)
+    check_route(logits, bias, wl.ROUTER_ALIGN_TOPK)
+
+
+@pytest.mark.parametrize("shape", [wl.TINY, wl.EP8_DECODE, wl.TP8_DECODE, wl.EP8_PREFILL],
+                         ids=lambda s: s.name)
+def test_route_layer_workloads(shape):
+    logits, bias = wl.router_inputs(shape.M, shape.E_total, shape.seed, shape.zipf)
+    check_route(logits, bias, shape.topk)
+
+
+@pytest.mark.parametrize("M,E,k", [(7, 1, 1), (5, 33, 32), (9, 64, 6), (3, 1000, 17), (33, 256, 8)])
+def test_route_odd_shapes(M, E, k):
+    logits, bias = wl.router_inputs(M, E, 21)
+    check_route(logits, bias, k)
+
+
+def test_route_special_values():
+    vals = np.float32([0.0, -0.0, 87.0, -87.0, 88.0, -88.0, 100.0, -100.0, 1e-30, -1e-30, 17.0,
+                       -17.0, 0.5, -0.5, 3e38, -3e38])
+    logits = np.tile(vals, (4, 24)).astype(np.float32)            # 384 columns, many ties
+    bias = np.zeros(384, np.float32)
+    bias[::7] = 0.1
+    bias[::11] = -0.05
+    check_route(logits, bias, 8)
+    # sweep the sigmoid through the weights of a top-32 route over 32 experts
+    x = np.linspace(-90, 90, 64 * 32, dtype=np.float32).reshape(64, 32)
+    check_route(x, np.zeros(32, np.float32), 32)
+
+
+def test_route_empty():
+    gw, gids = gpu_route(np.zeros((0, 384), np.float32), np.zeros(384, np.float32), 8)
+    assert gw.shape == (0, 8)
+
+
+def gpu_align(ids_np, begin, E_local, bm, M=None):
+    M = ids_np.shape[0] if M is None else M
+    k = ids_np.shape[1]
+    cap = chord.chord_moe_align_capacity(M, k, E_local, bm)
+    dev = "cuda"
+    ids = torch.from_numpy(np.ascontiguousarray(ids_np, np.int32)).to(dev)
+    st = torch.full((max(cap, 1),), -7, dtype=torch.int32, device=dev)
+    eid = torch.full((max(cap // bm, 1),), -7, dtype=torch.int32, device=dev)
+    ntpp = torch.full((1,), -7, dtype=torch.int32, device=dev)
+    cnt = torch.full((E_local,), -7, dtype=torch.int32, device=dev)
+    off = torch.full((E_local + 1,), -7, dtype=torch.int32, device=dev)
+    pos = torch.full((max(M * k, 1),), -7, dtype=torch.int32, device=dev)
+    wsb = chord.chord_moe_align_workspace_bytes(M, k, E_local)
+    ws = torch.full((max(wsb, 16),), 0x5A, dtype=torch.uint8, device=dev) if wsb else None
+    chord.chord_moe_align(ids, begin, E_local, bm, st[:cap] if cap else st, eid, ntpp, cnt, off,
+                          pos, ws)
+    torch.cuda.synchronize()
+    n = int(ntpp.item())
+    return dict(sorted_token_ids=st.cpu().numpy()[:n], expert_ids=eid.cpu().numpy()[:n // bm],
+                num_tokens_post_padded=n, expert_counts=cnt.cpu().numpy(),
+                expert_offsets=off.cpu().numpy(), sorted_positions=pos.cpu().numpy()[:M * k])
+
+
+def check_align(ids_np, begin, E_local, bm):
+    ref = oracle.moe_align(ids_np, begin, E_local, bm)
+    for _ in range(2):
+        got = gpu_align(ids_np, begin, E_local, bm)
+        assert got["num_tokens_post_padded"] == ref["num_tokens_post_padded"]
+        for key in ("expert_counts", "expert_offsets", "sorted_token_ids", "expert_ids",
+                    "sorted_positions"):
+            assert np.array_equal(got[key], ref[key]), key
+
+
+@pytest.mark.parametrize("M", wl.ROUTER_ALIGN_M)
+@pytest.mark.parametrize("bm", wl.ROUTER_ALIGN_BM)
+def test_align_router_workload(M, bm):
+    logits, bias = wl.router_inputs(M, wl.ROUTER_ALIGN_E, wl.ROUTER_ALIGN_SEED)
+    _, ids, _ = oracle.route(logits, bias, wl.ROUTER_ALIGN_TOPK)
+    check_align(ids, 0, wl.ROUTER_ALIGN_E, bm)
+
+
+@pytest.mark.parametrize("shape", [wl.TINY, wl.EP8_DECODE, wl.TP8_DECODE, wl.EP8_PREFILL],
+                         ids=lambda s: s.name)
+def test_align_layer_workloads(shape):
+    logits, bias = wl.router_inputs(shape.M, shape.E_total, shape.seed, shape.zipf)
+    _, ids, _ = oracle.route(logits, bias, shape.topk)
+    check_align(ids, shape.expert_begin, shape.E_local, 16)
+
+
+@pytest.mark.parametrize("M,k,E,begin,E_local,bm", [
+    (1000, 8, 384, 96, 48, 8),      # two chunks, ragged, EP shard
+    (513, 8, 384, 0, 384, 32),      # just over one chunk
+    (3, 2, 4, 0, 4, 128),
+    (40, 4, 1024, 0, 1024, 16),     # widest shard
+    (6000, 6, 16, 0, 16, 64),       # heavy per-expert counts over 9 chunks
+])
+def test_align_edge_shapes(M, k, E, begin, E_local, bm):
+    logits, bias = wl.router_inputs(M, E, 31)
+    _, ids, _ = oracle.route(logits, bias, k)
+    check_align(ids, begin, E_local, bm)
+
+
+def test_align_all_dropped_and_empty():
+    ids = np.array([[0, 1], [1, 2]], np.int32)
+    check_align(ids, 10, 4, 16)
+    got = gpu_align(np.zeros((0, 8), np.int32), 0, 384, 16)
+    assert got["num_tokens_post_padded"] == 0 and np.all(got["expert_counts"] == 0)
+    assert np.all(got["expert_offsets"] == 0)

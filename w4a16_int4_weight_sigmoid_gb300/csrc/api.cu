@@ -1,0 +1,302 @@
+// C ABI of the chord_moe library: argument checks, workspace carving, path
+// selection and launches.  No entry point allocates memory or synchronises.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "chord_moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(CHORD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool valid_block_m(int bm) { return bm == 8 || bm == 16 || bm == 32 || bm == 64 || bm == 128; }
+
+int check_tuning(const chord_tuning* t) {
+  if (!t) return CHORD_OK;
+  if (t->use_f16_accum)
+    return fail(CHORD_ERR_UNSUPPORTED, "FP16 accumulation is not implemented (FP32 only)");
+  if (t->batch_invariant)
+    return fail(CHORD_ERR_UNSUPPORTED, "batch-invariant mode is not implemented");
+  if (t->path < CHORD_PATH_AUTO || t->path > CHORD_PATH_LARGE_M)
+    return fail(CHORD_ERR_INVALID_ARG, "unknown path %d", t->path);
+  if (t->path == CHORD_PATH_LARGE_M)
+    return fail(CHORD_ERR_UNSUPPORTED, "large-M path not available in this build");
+  if (t->rows_per_pass != 0 && t->rows_per_pass != 8 && t->rows_per_pass != 16 && t->rows_per_pass != 32)
+    return fail(CHORD_ERR_INVALID_ARG, "rows_per_pass=%d not in {0, 8, 16, 32}", t->rows_per_pass);
+  return CHORD_OK;
+}
+
+// Token rows streamed per weight pass on the small-M path, from the expected
+// rows per expert.
+int rows_per_pass_for(double tok_e) {
+  if (tok_e <= 6.0) return 8;
+  if (tok_e <= 14.0) return 16;
+  return 32;
+}
+
+constexpr int kLayerBlockM = 16;
+
+struct LayerWs {
+  size_t tw, ids, sorted, eids, ntpp, counts, offsets, pos, align_ws, h, y, total;
+  size_t cap;
+};
+
+LayerWs layer_ws(int M, int H, int I, int E_local, int topk) {
+  LayerWs w{};
+  const size_t mk = static_cast<size_t>(M) * topk;
+  w.cap = chord_moe_align_capacity(M, topk, E_local, kLayerBlockM);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = round_up(o + bytes, 256);
+    return at;
+  };
+  w.tw = take(mk * sizeof(float));
+  w.ids = take(mk * sizeof(int32_t));
+  w.sorted = take(w.cap * sizeof(int32_t));
+  w.eids = take(w.cap / kLayerBlockM * sizeof(int32_t));
+  w.ntpp = take(sizeof(int32_t));
+  w.counts = take(static_cast<size_t>(E_local) * sizeof(int32_t));
+  w.offsets = take(static_cast<size_t>(E_local + 1) * sizeof(int32_t));
+  w.pos = take(mk * sizeof(int32_t));
+  w.align_ws = take(chord::align_workspace_bytes(static_cast<long long>(mk), E_local));
+  w.h = take(w.cap * static_cast<size_t>(I) * 2);
+  w.y = take(w.cap * static_cast<size_t>(H) * 2);
+  w.total = o;
+  return w;
+}
+
+int check_gemm_shapes(int N, int K, int epilogue) {
+  if (K <= 0 || K % 64 != 0) return fail(CHORD_ERR_INVALID_ARG, "K=%d must be a positive multiple of 64", K);
+  if (N <= 0 || N % 16 != 0) return fail(CHORD_ERR_INVALID_ARG, "N=%d must be a positive multiple of 16", N);
+  if (epilogue != CHORD_EPI_STORE && epilogue != CHORD_EPI_SILU_MUL)
+    return fail(CHORD_ERR_INVALID_ARG, "unknown epilogue %d", epilogue);
+  if (epilogue == CHORD_EPI_SILU_MUL && N % 128 != 0)
+    return fail(CHORD_ERR_INVALID_ARG, "SiLU*mul needs N=2I with I %% 64 == 0 (N=%d)", N);
+  return CHORD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* chord_last_error_string(void) { return g_err; }
+
+int chord_version(void) { return 100; }
+
+int chord_moe_route(const float* logits, const float* bias, int M, int E_total, int topk,
+                    float* topk_weights, int32_t* topk_ids, void* stream) {
+  if (M < 0) return fail(CHORD_ERR_INVALID_ARG, "M=%d < 0", M);
+  if (E_total < 1 || E_total > 1024) return fail(CHORD_ERR_INVALID_ARG, "E_total=%d not in [1, 1024]", E_total);
+  if (topk < 1 || topk > E_total || topk > 32)
+    return fail(CHORD_ERR_INVALID_ARG, "topk=%d not in [1, min(E_total, 32)]", topk);
+  if (M > 0 && (!logits || !bias || !topk_weights || !topk_ids))
+    return fail(CHORD_ERR_INVALID_ARG, "null pointer");
+  cudaError_t e = chord::route_launch(logits, bias, M, E_total, topk, topk_weights, topk_ids,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "route launch");
+}
+
+size_t chord_moe_align_capacity(int M, int topk, int E_local, int block_m) {
+  if (M < 0 || topk < 1 || E_local < 1 || !valid_block_m(block_m)) return 0;
+  const size_t R = static_cast<size_t>(M) * topk;
+  const size_t cap = R + (R < static_cast<size_t>(E_local) ? R : E_local) * (block_m - 1);
+  return round_up(cap, block_m);
+}
+
+size_t chord_moe_align_workspace_bytes(int M, int topk, int E_local) {
+  if (M < 0 || topk < 1 || E_local < 1) return 0;
+  return chord::align_workspace_bytes(static_cast<long long>(M) * topk, E_local);
+}
+
+int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, int E_local,
+                    int block_m, size_t capacity, int32_t* sorted_token_ids, int32_t* expert_ids,
+                    int32_t* num_tokens_post_padded, int32_t* expert_counts,
+                    int32_t* expert_offsets, int32_t* sorted_positions, void* workspace,
+                    size_t ws_bytes, void* stream) {
+  if (M < 0 || topk < 1 || topk > 32) return fail(CHORD_ERR_INVALID_ARG, "bad M=%d or topk=%d", M, topk);
+  if (E_local < 1 || E_local > 1024) return fail(CHORD_ERR_INVALID_ARG, "E_local=%d not in [1, 1024]", E_local);
+  if (expert_begin < 0) return fail(CHORD_ERR_INVALID_ARG, "expert_begin=%d < 0", expert_begin);
+  if (!valid_block_m(block_m)) return fail(CHORD_ERR_INVALID_ARG, "block_m=%d not in {8,16,32,64,128}", block_m);
+  if (static_cast<long long>(M) * topk > (1LL << 30)) return fail(CHORD_ERR_INVALID_ARG, "M*topk too large");
+  const size_t need = chord_moe_align_capacity(M, topk, E_local, block_m);
+  if (capacity < need) return fail(CHORD_ERR_INVALID_ARG, "capacity %zu < required %zu", capacity, need);
+  if (!expert_ids || !num_tokens_post_padded || !expert_counts || !expert_offsets || !sorted_token_ids ||
+      (M > 0 && !topk_ids))
+    return fail(CHORD_ERR_INVALID_ARG, "null pointer");
+  const size_t wneed = chord_moe_align_workspace_bytes(M, topk, E_local);
+  if (ws_bytes < wneed || (wneed > 0 && !workspace))
+    return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "align workspace %zu < required %zu", ws_bytes, wneed);
+  cudaError_t e = chord::align_launch(topk_ids, M, topk, expert_begin, E_local, block_m,
+                                      sorted_token_ids, expert_ids, num_tokens_post_padded,
+                                      expert_counts, expert_offsets, sorted_positions, workspace,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "align launch");
+}
+
+size_t chord_w4a16_prepack_bytes(int E, int N, int K, int group) {
+  if (E < 1 || N < 1 || K < 64 || K % 64 != 0 || group != 32) return 0;
+  return chord::prepack_bytes(E, N, K);
+}
+
+int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E, int N, int K,
+                        int group, int gate_up, void* packed, size_t packed_bytes, void* stream) {
+  if (group != 32) return fail(CHORD_ERR_UNSUPPORTED, "group=%d: only group-32 scales are implemented", group);
+  if (E < 1) return fail(CHORD_ERR_INVALID_ARG, "E=%d < 1", E);
+  if (K <= 0 || K % 64 != 0) return fail(CHORD_ERR_INVALID_ARG, "K=%d must be a positive multiple of 64", K);
+  if (N <= 0 || N % 16 != 0) return fail(CHORD_ERR_INVALID_ARG, "N=%d must be a positive multiple of 16", N);
+  if (gate_up && N % 128 != 0) return fail(CHORD_ERR_INVALID_ARG, "gate_up needs N %% 128 == 0 (N=%d)", N);
+  if (!qweight || !scales || !packed) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(packed)) return fail(CHORD_ERR_INVALID_ARG, "packed must be 16-byte aligned");
+  const size_t need = chord_w4a16_prepack_bytes(E, N, K, group);
+  if (packed_bytes < need) return fail(CHORD_ERR_INVALID_ARG, "packed_bytes %zu < required %zu", packed_bytes, need);
+  cudaError_t e = chord::prepack_launch(qweight, scales, E, N, K, gate_up != 0,
+                                        static_cast<uint8_t*>(packed), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "prepack launch");
+}
+
+static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, int E_local, int N,
+                     int K, int M, int topk, const int32_t* sorted_token_ids,
+                     const int32_t* expert_counts, const int32_t* expert_offsets, int epilogue,
+                     chord_bf16* C, const chord_tuning* tuning, double tok_e, int* dev_status,
+                     void* stream) {
+  int rc = check_tuning(tuning);
+  if (rc) return rc;
+  rc = check_gemm_shapes(N, K, epilogue);
+  if (rc) return rc;
+  if (E_local < 1 || M < 0 || topk < 1) return fail(CHORD_ERR_INVALID_ARG, "bad E_local/M/topk");
+  if (!A || !packed_w || !C || !expert_counts || !expert_offsets || (a_gather && !sorted_token_ids))
+    return fail(CHORD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(A) || !aligned16(packed_w)) return fail(CHORD_ERR_INVALID_ARG, "A and packed_w must be 16-byte aligned");
+  if (M == 0) return CHORD_OK;
+  chord::GemmLaunch g;
+  g.A = A;
+  g.gather = a_gather != 0;
+  g.packed = packed_w;
+  g.E_local = E_local;
+  g.N = N;
+  g.K = K;
+  g.M = M;
+  g.topk = topk;
+  g.sorted = sorted_token_ids;
+  g.counts = expert_counts;
+  g.offsets = expert_offsets;
+  g.epilogue = epilogue;
+  g.C = C;
+  g.status = dev_status;
+  const int rpp = tuning && tuning->rows_per_pass ? tuning->rows_per_pass : rows_per_pass_for(tok_e);
+  cudaError_t e = chord::gemm_small_launch(g, rpp, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "gemm launch");
+}
+
+int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w, int E_local,
+                         int N, int K, int M, int topk, const int32_t* sorted_token_ids,
+                         const int32_t* expert_counts, const int32_t* expert_offsets,
+                         size_t capacity, int epilogue, chord_bf16* C, const chord_tuning* tuning,
+                         int* dev_status, void* stream) {
+  (void)capacity;
+  const double tok_e = E_local > 0 ? static_cast<double>(M) * topk / E_local : 0.0;
+  return gemm_impl(A, a_gather, packed_w, E_local, N, K, M, topk, sorted_token_ids, expert_counts,
+                   expert_offsets, epilogue, C, tuning, tok_e, dev_status, stream);
+}
+
+int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions,
+                  int M, int topk, int H, chord_bf16* out, void* stream) {
+  if (M < 0 || topk < 1 || H <= 0 || H % 8 != 0) return fail(CHORD_ERR_INVALID_ARG, "bad M/topk/H (H %% 8 == 0)");
+  if (M > 0 && (!y || !topk_weights || !sorted_positions || !out)) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(y) || !aligned16(out)) return fail(CHORD_ERR_INVALID_ARG, "y and out must be 16-byte aligned");
+  cudaError_t e = chord::moe_sum_launch(y, topk_weights, sorted_positions, M, topk, H, out,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "moe_sum launch");
+}
+
+int chord_moe_layer_plan(int M, int E_total, int topk, chord_tuning* plan) {
+  if (!plan || M < 0 || E_total < 1 || topk < 1) return fail(CHORD_ERR_INVALID_ARG, "bad plan arguments");
+  const double tok_e = static_cast<double>(M) * topk / E_total;
+  plan->path = CHORD_PATH_SMALL_M;
+  plan->rows_per_pass = rows_per_pass_for(tok_e);
+  plan->use_f16_accum = 0;
+  plan->batch_invariant = 0;
+  return CHORD_OK;
+}
+
+size_t chord_moe_layer_workspace_bytes(int M, int H, int I, int E_local, int topk) {
+  if (M < 0 || H <= 0 || I <= 0 || E_local < 1 || topk < 1) return 0;
+  return layer_ws(M, H, I, E_local, topk).total;
+}
+
+int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
+                    const void* w13_packed, const void* w2_packed, int M, int H, int I,
+                    int E_total, int expert_begin, int E_local, int topk, chord_bf16* out,
+                    float* topk_weights_out, int32_t* topk_ids_out, void* workspace,
+                    size_t ws_bytes, const chord_tuning* tuning, int* dev_status, void* stream) {
+  int rc = check_tuning(tuning);
+  if (rc) return rc;
+  if (M < 0) return fail(CHORD_ERR_INVALID_ARG, "M=%d < 0", M);
+  if (H <= 0 || H % 64 != 0) return fail(CHORD_ERR_INVALID_ARG, "H=%d must be a positive multiple of 64", H);
+  if (I <= 0 || I % 64 != 0) return fail(CHORD_ERR_INVALID_ARG, "I=%d must be a positive multiple of 64", I);
+  if (E_local < 1 || expert_begin < 0 || expert_begin + E_local > E_total)
+    return fail(CHORD_ERR_INVALID_ARG, "local experts [%d, %d) not within E_total=%d", expert_begin,
+                expert_begin + E_local, E_total);
+  if (M == 0) return CHORD_OK;
+  if (!x || !logits || !bias || !w13_packed || !w2_packed || !out || !workspace)
+    return fail(CHORD_ERR_INVALID_ARG, "null pointer");
+  const LayerWs w = layer_ws(M, H, I, E_local, topk);
+  if (ws_bytes < w.total) return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "layer workspace %zu < required %zu", ws_bytes, w.total);
+  if (!aligned16(workspace)) return fail(CHORD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  char* ws = static_cast<char*>(workspace);
+  float* tw = topk_weights_out ? topk_weights_out : reinterpret_cast<float*>(ws + w.tw);
+  int32_t* ids = topk_ids_out ? topk_ids_out : reinterpret_cast<int32_t*>(ws + w.ids);
+  int32_t* sorted = reinterpret_cast<int32_t*>(ws + w.sorted);
+  int32_t* eids = reinterpret_cast<int32_t*>(ws + w.eids);
+  int32_t* ntpp = reinterpret_cast<int32_t*>(ws + w.ntpp);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + w.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + w.offsets);
+  int32_t* pos = reinterpret_cast<int32_t*>(ws + w.pos);
+  void* aws = ws + w.align_ws;
+  chord_bf16* h = reinterpret_cast<chord_bf16*>(ws + w.h);
+  chord_bf16* y = reinterpret_cast<chord_bf16*>(ws + w.y);
+
+  rc = chord_moe_route(logits, bias, M, E_total, topk, tw, ids, stream);
+  if (rc) return rc;
+  rc = chord_moe_align(ids, M, topk, expert_begin, E_local, kLayerBlockM, w.cap, sorted, eids, ntpp,
+                       counts, offsets, pos, aws,
+                       chord_moe_align_workspace_bytes(M, topk, E_local), stream);
+  if (rc) return rc;
+  chord_tuning plan;
+  chord_moe_layer_plan(M, E_total, topk, &plan);
+  if (tuning) {
+    if (tuning->path) plan.path = tuning->path;
+    if (tuning->rows_per_pass) plan.rows_per_pass = tuning->rows_per_pass;
+  }
+  tuning = &plan;
+  const double tok_e = static_cast<double>(M) * topk / E_total;
+  rc = gemm_impl(x, 1, w13_packed, E_local, 2 * I, H, M, topk, sorted, counts, offsets,
+                 CHORD_EPI_SILU_MUL, h, tuning, tok_e, dev_status, stream);
+  if (rc) return rc;
+  rc = gemm_impl(h, 0, w2_packed, E_local, H, I, M, topk, sorted, counts, offsets, CHORD_EPI_STORE,
+                 y, tuning, tok_e, dev_status, stream);
+  if (rc) return rc;
+  return chord_moe_sum(y, tw, pos, M, topk, H, out, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,153 @@
+// Device-side helpers shared by the chord_moe kernels (sm_103a).
+//
+// Inline PTX for mbarriers, bulk async copies (TMA 1D), ldmatrix and the
+// register-operand BF16 MMA, plus bounded waits: every spin on an mbarrier
+// gives up after a fixed number of polls, records CHORD_ERR_TIMEOUT in the
+// caller's status word and lets the kernel return.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "chord_moe.h"
+
+namespace chord {
+
+constexpr int kGroup = 32;            // INT4 scale group along K
+constexpr int kTileRows = 128;        // weight rows per packed tile
+constexpr int kUnitK = 64;            // K per packed unit
+constexpr int kUnitQBytes = kTileRows * kUnitK / 2;          // 4096
+constexpr int kUnitSBytes = kTileRows * (kUnitK / kGroup) * 2; // 512
+constexpr int kUnitBytes = kUnitQBytes + kUnitSBytes;        // 4608
+constexpr uint32_t kPackMagic = 0x57344843u;   // "CH4W"
+constexpr uint32_t kPackVersion = 1u;
+constexpr int kPackHeaderBytes = 256;
+constexpr uint32_t kPackFlagGateUp = 1u;
+
+// Packed-weight header (first 256 bytes of a prepacked blob).
+struct PackHeader {
+  uint32_t magic, version;
+  int32_t E, N, K, group, tile_rows, unit_k;
+  uint32_t flags;
+  int32_t n_tiles;
+  int64_t tile_bytes;   // bytes of one 128-row tile over all of K
+  int64_t expert_bytes; // n_tiles * tile_bytes
+};
+static_assert(sizeof(PackHeader) <= kPackHeaderBytes, "header too large");
+
+__device__ __forceinline__ void set_status(int* st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Poll limit: each try_wait may suspend the thread for a while, so this is
+// seconds of waiting, far beyond any legitimate stall.
+constexpr uint32_t kWaitPolls = 1u << 24;
+
+// Returns false (and records a timeout) if the phase did not complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  set_status(status, CHORD_ERR_TIMEOUT);
+  return false;
+}
+
+// ------------------------------------------------------- bulk async copies
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- MMA
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D = A(16x16, row) * B(16x8, col) + C, BF16 inputs, FP32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
+}
+
+// ------------------------------------------------------------ INT4 decode
+// A packed word holds 8 offset-binary nibbles u = q + 8.  Nibble positions
+// j and j+4 form register j of an m16n8k16 A fragment: (128 + u) is built by
+// OR-ing the nibble into the mantissa of BF16 128.0, then 136 is subtracted,
+// leaving q exactly.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t kMagic = 0x43004300u;  // bf16x2 (128, 128)
+  const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.f, 136.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | kMagic;
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
+    h = __hsub2(h, k136);
+    a[j] = *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (the first
+// call must precede any stream capture; later calls make no CUDA call).
+template <typename Kern>
+inline cudaError_t ensure_smem_limit(Kern kern, int bytes) {
+  static int done_bytes[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done_bytes[dev] >= bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) done_bytes[dev] = bytes;
+  return err;
+}
+
+}  // namespace chord

@@ -1,0 +1,43 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace chord {
+
+struct PackHeader;
+
+cudaError_t route_launch(const float* logits, const float* bias, int M, int E, int topk, float* w,
+                         int32_t* ids, cudaStream_t st);
+
+int align_num_chunks(long long n);
+size_t align_workspace_bytes(long long n, int E_local);
+cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_local, int bm,
+                         int32_t* sorted, int32_t* expert_ids, int32_t* ntpp, int32_t* counts,
+                         int32_t* offsets, int32_t* positions, void* ws, cudaStream_t st);
+
+PackHeader make_pack_header(int E, int N, int K, bool gate_up);
+size_t prepack_bytes(int E, int N, int K);
+cudaError_t prepack_launch(const uint8_t* q, const uint16_t* s, int E, int N, int K, bool gate_up,
+                           uint8_t* out, cudaStream_t st);
+
+struct GemmLaunch {
+  const uint16_t* A;
+  bool gather;
+  const void* packed;
+  int E_local, N, K, M, topk;
+  const int32_t* sorted;
+  const int32_t* counts;
+  const int32_t* offsets;
+  int epilogue;
+  uint16_t* C;
+  int* status;
+};
+cudaError_t gemm_small_launch(const GemmLaunch& g, int rows_per_pass, cudaStream_t st);
+
+cudaError_t moe_sum_launch(const uint16_t* y, const float* w, const int32_t* pos, int M, int topk,
+                           int H, uint16_t* out, cudaStream_t st);
+
+}  // namespace chord

@@ -1,0 +1,53 @@
+// Top-k weighted sum of expert outputs back to tokens (moe_fused_mul_sum,
+// [HumPR] "왜 이게 좋은가" 3).  out[t] = sum_j w[t,j] * y[pos(t,j)], FP32 in
+// increasing j, one rounding to BF16; 16-byte vector loads and stores.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace chord {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kColsPerCta = kThreads * 8;
+
+__global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* __restrict__ y,
+                                                           const float* __restrict__ w,
+                                                           const int32_t* __restrict__ pos,
+                                                           int topk, int H,
+                                                           uint16_t* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int c = blockIdx.y * kColsPerCta + threadIdx.x * 8;
+  if (c >= H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int j = 0; j < topk; ++j) {
+    const int p = __ldg(pos + static_cast<size_t>(t) * topk + j);
+    if (p < 0) continue;
+    const float wj = __ldg(w + static_cast<size_t>(t) * topk + j);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(p) * H + c));
+    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(wj, bf16lo_to_f32(vv[i]), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wj, bf16hi_to_f32(vv[i]), acc[2 * i + 1]);
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = uint32_t(f32_to_bf16_rn(acc[2 * i])) | (uint32_t(f32_to_bf16_rn(acc[2 * i + 1])) << 16);
+  *reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+}  // namespace
+
+cudaError_t moe_sum_launch(const uint16_t* y, const float* w, const int32_t* pos, int M, int topk,
+                           int H, uint16_t* out, cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  dim3 grid(M, (H + kColsPerCta - 1) / kColsPerCta);
+  moe_sum_kernel<<<grid, kThreads, 0, st>>>(y, w, pos, topk, H, out);
+  return cudaGetLastError();
+}
+
+}  // namespace chord
