@@ -264,9 +264,9 @@ cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_l
   a.ws_counts = a.ws_rank ? a.ws_rank + a.n : nullptr;
   const size_t smem = align_smem_bytes(E_local);
   const int max_smem = static_cast<int>(align_smem_bytes(1024));
-  cudaError_t err = ensure_smem_limit(align_single_kernel, max_smem);
-  if (err == cudaSuccess) err = ensure_smem_limit(align_rank_kernel, max_smem);
-  if (err == cudaSuccess) err = ensure_smem_limit(align_scatter_kernel, max_smem);
+  cudaError_t err = ensure_smem_limit<align_single_kernel>(max_smem);
+  if (err == cudaSuccess) err = ensure_smem_limit<align_rank_kernel>(max_smem);
+  if (err == cudaSuccess) err = ensure_smem_limit<align_scatter_kernel>(max_smem);
   if (err != cudaSuccess) return err;
   if (a.G == 1) {
     align_single_kernel<<<1, kThreads, smem, st>>>(a);

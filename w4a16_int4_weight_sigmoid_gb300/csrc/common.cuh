@@ -135,17 +135,18 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// Raise a kernel's dynamic shared-memory limit once per device (the first
-// call must precede any stream capture; later calls make no CUDA call).
-template <typename Kern>
-inline cudaError_t ensure_smem_limit(Kern kern, int bytes) {
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device):
+// the first call must precede any stream capture; later calls make no CUDA
+// call.  Keyed by the kernel itself (a template argument), not its type.
+template <auto Kern>
+inline cudaError_t ensure_smem_limit(int bytes) {
   static int done_bytes[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (done_bytes[dev] >= bytes) return cudaSuccess;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  err = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err == cudaSuccess) done_bytes[dev] = bytes;
   return err;
 }

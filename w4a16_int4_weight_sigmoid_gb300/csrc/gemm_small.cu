@@ -249,7 +249,7 @@ template <int NT, int STAGES, bool GATHER, int EPI>
 cudaError_t launch_small(const SmallArgs& a, cudaStream_t st) {
   auto kern = gemm_small_kernel<NT, STAGES, GATHER, EPI>;
   const int smem = STAGES * SmallCfg<NT>::kStageBytes;
-  cudaError_t err = ensure_smem_limit(kern, smem);
+  cudaError_t err = ensure_smem_limit<gemm_small_kernel<NT, STAGES, GATHER, EPI>>(smem);
   if (err != cudaSuccess) return err;
   dim3 grid(a.n_tiles, a.E_local);
   kern<<<grid, kThreads, smem, st>>>(a);
