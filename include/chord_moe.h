@@ -134,6 +134,36 @@ int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, 
                     int32_t* expert_offsets, int32_t* sorted_positions, void* workspace,
                     size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of chord_moe_align.  The pages have no counterpart;
+ * it exists for callers that cannot allocate device memory at all: code
+ * running under an engine or plugin that owns every device allocation and
+ * hands out no scratch, or a hot path where cudaMalloc is not allowed (it can
+ * synchronise the device and is forbidden while a stream is being captured).
+ * Arguments, outputs and results are those of chord_moe_align; the only
+ * difference is where the scratch lives: when M*topk > 4096 the align needs
+ * per-assignment ranks and per-chunk counts, and this entry point keeps them
+ * in one static device array inside the library (320 KiB, held by every GPU
+ * that loads the library until the process exits) instead of a workspace.
+ *   Limits: M*topk <= CHORD_ALIGN_NOALLOC_MAX_ASSIGNMENTS and
+ *   E_local <= CHORD_ALIGN_NOALLOC_MAX_EXPERTS; larger calls return
+ *   CHORD_ERR_INVALID_ARG and launch nothing.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture.  It allocates nothing and calls no
+ *   cudaMalloc/cudaFree.
+ *   Sharing: all calls use the same array and it keeps the last call's
+ *   contents (every call rewrites what it reads, so nothing needs clearing);
+ *   calls whose executions overlap on the GPU (other streams, other threads)
+ *   race on it and must be serialised by the caller.
+ */
+#define CHORD_ALIGN_NOALLOC_MAX_ASSIGNMENTS 65536
+#define CHORD_ALIGN_NOALLOC_MAX_EXPERTS 1024
+int chord_moe_align_noalloc(const int32_t* topk_ids, int M, int topk, int expert_begin, int E_local,
+                            int block_m, size_t capacity, int32_t* sorted_token_ids,
+                            int32_t* expert_ids, int32_t* num_tokens_post_padded,
+                            int32_t* expert_counts, int32_t* expert_offsets,
+                            int32_t* sorted_positions, void* stream);
+
 /* ---------------------------------------------------------------- prepack
  * Repack INT4 weights and scales into this library's kernel layout
  * ([Humming] "워크로드별 튜닝 및 JIT 컴파일": preprocessing validates

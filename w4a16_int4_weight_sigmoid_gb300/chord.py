@@ -53,6 +53,7 @@ _SIGS = {
     "chord_moe_align_capacity": (_Z, [_I, _I, _I, _I]),
     "chord_moe_align_workspace_bytes": (_Z, [_I, _I, _I]),
     "chord_moe_align": (_I, [_P, _I, _I, _I, _I, _I, _Z, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "chord_moe_align_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _Z, _P, _P, _P, _P, _P, _P, _P]),
     "chord_w4a16_prepack_bytes": (_Z, [_I, _I, _I, _I]),
     "chord_w4a16_prepack": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "chord_w4a16_moe_gemm": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _I, _P, _P,
@@ -148,6 +149,21 @@ def chord_moe_align(topk_ids, expert_begin: int, E_local: int, block_m: int, sor
         _ptr(expert_counts, i32, "expert_counts"), _ptr(expert_offsets, i32, "expert_offsets"),
         _ptr(sorted_positions, i32, "sorted_positions"), _ptr(workspace, None, "workspace"),
         ws_bytes, _stream(stream)))
+
+
+def chord_moe_align_noalloc(topk_ids, expert_begin: int, E_local: int, block_m: int,
+                            sorted_token_ids, expert_ids, num_tokens_post_padded, expert_counts,
+                            expert_offsets, sorted_positions=None, stream=None):
+    """chord_moe_align without a workspace argument: for callers that cannot
+    allocate device memory; its scratch is a static array in the library."""
+    M, k = topk_ids.shape
+    i32 = torch.int32
+    _check(lib().chord_moe_align_noalloc(
+        _ptr(topk_ids, i32, "topk_ids"), M, k, expert_begin, E_local, block_m,
+        sorted_token_ids.numel(), _ptr(sorted_token_ids, i32, "sorted_token_ids"),
+        _ptr(expert_ids, i32, "expert_ids"), _ptr(num_tokens_post_padded, i32, "ntpp"),
+        _ptr(expert_counts, i32, "expert_counts"), _ptr(expert_offsets, i32, "expert_offsets"),
+        _ptr(sorted_positions, i32, "sorted_positions"), _stream(stream)))
 
 
 def chord_w4a16_prepack_bytes(E: int, N: int, K: int, group: int = 32) -> int:

@@ -280,3 +280,44 @@ cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_l
 }
 
 }  // namespace chord
+
+// ---------------------------------------------------------------------------
+// Allocation-free align: the scratch of the multi-chunk path (per-assignment
+// chunk ranks, then per-chunk expert counts) lives in this file-scope device
+// array instead of a caller-provided workspace.  Every GPU that loads the
+// library holds it (320 KiB) until the process exits.
+namespace chord {
+
+constexpr long long kNoAllocMaxAssignments = CHORD_ALIGN_NOALLOC_MAX_ASSIGNMENTS;
+constexpr int kNoAllocMaxExperts = CHORD_ALIGN_NOALLOC_MAX_EXPERTS;
+constexpr long long kNoAllocScratchInts =
+    kNoAllocMaxAssignments +
+    ((kNoAllocMaxAssignments + kChunk - 1) / kChunk) * static_cast<long long>(kNoAllocMaxExperts);
+
+static __device__ __align__(256) int32_t g_align_scratch[kNoAllocScratchInts];
+
+namespace {
+// Device address of g_align_scratch, looked up once per device.  In host code
+// the symbol name is only a host-side stand-in, so it is never passed to a
+// kernel directly.
+void* g_scratch_ptr[64] = {nullptr};
+}  // namespace
+
+cudaError_t align_noalloc_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_align_scratch);
+    if (err != cudaSuccess) return err;
+    g_scratch_ptr[dev] = p;
+  }
+  *ptr = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+size_t align_noalloc_scratch_bytes() { return static_cast<size_t>(kNoAllocScratchInts) * sizeof(int32_t); }
+
+}  // namespace chord

@@ -153,6 +153,30 @@ int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, 
   return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "align launch");
 }
 
+int chord_moe_align_noalloc(const int32_t* topk_ids, int M, int topk, int expert_begin, int E_local,
+                            int block_m, size_t capacity, int32_t* sorted_token_ids,
+                            int32_t* expert_ids, int32_t* num_tokens_post_padded,
+                            int32_t* expert_counts, int32_t* expert_offsets,
+                            int32_t* sorted_positions, void* stream) {
+  if (M < 0 || topk < 1 || static_cast<long long>(M) * topk > CHORD_ALIGN_NOALLOC_MAX_ASSIGNMENTS)
+    return fail(CHORD_ERR_INVALID_ARG, "allocation-free align takes M*topk <= %d (got M=%d, topk=%d)",
+                CHORD_ALIGN_NOALLOC_MAX_ASSIGNMENTS, M, topk);
+  if (E_local < 1 || E_local > CHORD_ALIGN_NOALLOC_MAX_EXPERTS)
+    return fail(CHORD_ERR_INVALID_ARG, "allocation-free align takes 1 <= E_local <= %d (got %d)",
+                CHORD_ALIGN_NOALLOC_MAX_EXPERTS, E_local);
+  const size_t wneed = chord_moe_align_workspace_bytes(M, topk, E_local);
+  void* scratch = nullptr;
+  if (wneed > 0) {
+    if (wneed > chord::align_noalloc_scratch_bytes())
+      return fail(CHORD_ERR_INVALID_ARG, "scratch need %zu exceeds the static array", wneed);
+    cudaError_t e = chord::align_noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the align scratch");
+  }
+  return chord_moe_align(topk_ids, M, topk, expert_begin, E_local, block_m, capacity,
+                         sorted_token_ids, expert_ids, num_tokens_post_padded, expert_counts,
+                         expert_offsets, sorted_positions, scratch, wneed, stream);
+}
+
 size_t chord_w4a16_prepack_bytes(int E, int N, int K, int group) {
   if (E < 1 || N < 1 || K < 64 || K % 64 != 0 || group != 32) return 0;
   return chord::prepack_bytes(E, N, K);

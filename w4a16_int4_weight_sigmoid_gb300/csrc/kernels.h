@@ -18,6 +18,9 @@ cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_l
                          int32_t* sorted, int32_t* expert_ids, int32_t* ntpp, int32_t* counts,
                          int32_t* offsets, int32_t* positions, void* ws, cudaStream_t st);
 
+cudaError_t align_noalloc_scratch(void** ptr);
+size_t align_noalloc_scratch_bytes();
+
 PackHeader make_pack_header(int E, int N, int K, bool gate_up);
 size_t prepack_bytes(int E, int N, int K);
 cudaError_t prepack_launch(const uint8_t* q, const uint16_t* s, int E, int N, int K, bool gate_up,
