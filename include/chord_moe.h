@@ -175,8 +175,8 @@ int chord_moe_align_noalloc(const int32_t* topk_ids, int M, int topk, int expert
  *   gate_up  1: rows 0..N/2-1 are the gate projection and N/2..N-1 the up
  *            projection (required for CHORD_EPI_SILU_MUL); 0 otherwise
  *   packed   out, chord_w4a16_prepack_bytes() bytes, 16-byte aligned
- * Requires K % 64 == 0; N % 16 == 0 (gate_up: N % 128 == 0).  N is padded
- * to a multiple of 128 rows with zero weights.  The blob starts with a
+ * Requires K % 64 == 0; N % 16 == 0 (gate_up: N % 64 == 0).  N is padded
+ * to a multiple of 64 rows with zero weights.  The blob starts with a
  * 256-byte header (magic, version, shapes, flags) that every GEMM launch
  * checks on the device.
  */

@@ -56,8 +56,8 @@ def test_sizing_functions(L):
     assert L.chord_moe_align_capacity(1, 8, 384, 7) == 0           # bad block_m
     assert L.chord_moe_align_workspace_bytes(128, 8, 384) == 0      # one chunk: none
     assert L.chord_moe_align_workspace_bytes(4096, 8, 384) == (32768 + 8 * 384) * 4
-    assert L.chord_w4a16_prepack_bytes(48, 4096, 7168, 32) == 256 + 48 * 32 * 112 * 4608
-    assert L.chord_w4a16_prepack_bytes(1, 16, 64, 32) == 256 + 4608
+    assert L.chord_w4a16_prepack_bytes(48, 4096, 7168, 32) == 256 + 48 * 64 * 112 * 2304
+    assert L.chord_w4a16_prepack_bytes(1, 16, 64, 32) == 256 + 2304
     assert L.chord_w4a16_prepack_bytes(1, 16, 96, 32) == 0          # K % 64
     assert L.chord_w4a16_prepack_bytes(1, 16, 64, 64) == 0          # group 64
     assert L.chord_moe_layer_workspace_bytes(64, 7168, 2048, 48, 8) > 0
@@ -90,7 +90,7 @@ def test_argument_checks_reject_before_launch(L):
     rc, _ = _rc_and_msg(L, L.chord_w4a16_prepack(P, P, 2, 128, 128, 128, 0, P, 10 ** 9, None))
     assert rc == chord.CHORD_ERR_UNSUPPORTED
     rc, _ = _rc_and_msg(L, L.chord_w4a16_prepack(P, P, 2, 96, 128, 32, 1, P, 10 ** 9, None))
-    assert rc == chord.CHORD_ERR_INVALID_ARG                        # gate_up needs N % 128
+    assert rc == chord.CHORD_ERR_INVALID_ARG                        # gate_up needs N % 64
     t = chord.chord_tuning(0, 0, 1, 0)
     rc, msg = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, 100, 0, P,
                                                     ctypes.byref(t), None, None))
@@ -102,9 +102,9 @@ def test_argument_checks_reject_before_launch(L):
     rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 100, 8, 2, P, P, P, 100, 0, P,
                                                   None, None, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # K % 64
-    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 192, 128, 8, 2, P, P, P, 100, 1, P,
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 96, 128, 8, 2, P, P, P, 100, 1, P,
                                                   None, None, None))
-    assert rc == chord.CHORD_ERR_INVALID_ARG                        # SiLU needs N % 128
+    assert rc == chord.CHORD_ERR_INVALID_ARG                        # SiLU needs N % 64
     rc, _ = _rc_and_msg(L, L.chord_moe_sum(P, P, P, 4, 2, 100, P, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # H % 8
     rc, _ = _rc_and_msg(L, L.chord_moe_layer(P, P, P, P, P, 4, 256, 128, 8, 4, 8, 2, P, None, None,

@@ -90,8 +90,8 @@ int check_gemm_shapes(int N, int K, int epilogue) {
   if (N <= 0 || N % 16 != 0) return fail(CHORD_ERR_INVALID_ARG, "N=%d must be a positive multiple of 16", N);
   if (epilogue != CHORD_EPI_STORE && epilogue != CHORD_EPI_SILU_MUL)
     return fail(CHORD_ERR_INVALID_ARG, "unknown epilogue %d", epilogue);
-  if (epilogue == CHORD_EPI_SILU_MUL && N % 128 != 0)
-    return fail(CHORD_ERR_INVALID_ARG, "SiLU*mul needs N=2I with I %% 64 == 0 (N=%d)", N);
+  if (epilogue == CHORD_EPI_SILU_MUL && N % 64 != 0)
+    return fail(CHORD_ERR_INVALID_ARG, "SiLU*mul needs N=2I with I %% 32 == 0 (N=%d)", N);
   return CHORD_OK;
 }
 
@@ -188,7 +188,7 @@ int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E,
   if (E < 1) return fail(CHORD_ERR_INVALID_ARG, "E=%d < 1", E);
   if (K <= 0 || K % 64 != 0) return fail(CHORD_ERR_INVALID_ARG, "K=%d must be a positive multiple of 64", K);
   if (N <= 0 || N % 16 != 0) return fail(CHORD_ERR_INVALID_ARG, "N=%d must be a positive multiple of 16", N);
-  if (gate_up && N % 128 != 0) return fail(CHORD_ERR_INVALID_ARG, "gate_up needs N %% 128 == 0 (N=%d)", N);
+  if (gate_up && N % 64 != 0) return fail(CHORD_ERR_INVALID_ARG, "gate_up needs N %% 64 == 0 (N=%d)", N);
   if (!qweight || !scales || !packed) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(packed)) return fail(CHORD_ERR_INVALID_ARG, "packed must be 16-byte aligned");
   const size_t need = chord_w4a16_prepack_bytes(E, N, K, group);

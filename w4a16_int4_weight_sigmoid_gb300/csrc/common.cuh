@@ -15,13 +15,14 @@
 namespace chord {
 
 constexpr int kGroup = 32;            // INT4 scale group along K
-constexpr int kTileRows = 128;        // weight rows per packed tile
+constexpr int kTileRows = 64;         // weight rows per packed tile (4 slabs of 16)
+constexpr int kSlabs = kTileRows / 16;
 constexpr int kUnitK = 64;            // K per packed unit
-constexpr int kUnitQBytes = kTileRows * kUnitK / 2;          // 4096
-constexpr int kUnitSBytes = kTileRows * (kUnitK / kGroup) * 2; // 512
-constexpr int kUnitBytes = kUnitQBytes + kUnitSBytes;        // 4608
+constexpr int kUnitQBytes = kTileRows * kUnitK / 2;          // 2048
+constexpr int kUnitSBytes = kTileRows * (kUnitK / kGroup) * 2; // 256
+constexpr int kUnitBytes = kUnitQBytes + kUnitSBytes;        // 2304
 constexpr uint32_t kPackMagic = 0x57344843u;   // "CH4W"
-constexpr uint32_t kPackVersion = 1u;
+constexpr uint32_t kPackVersion = 2u;
 constexpr int kPackHeaderBytes = 256;
 constexpr uint32_t kPackFlagGateUp = 1u;
 
@@ -82,6 +83,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   return false;
 }
 
+// Same, for a thread that is not latency critical (a producer waiting for a
+// free slot): sleeps briefly between probes instead of spinning.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, int* status) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    __nanosleep(64);
+  }
+  set_status(status, CHORD_ERR_TIMEOUT);
+  return false;
+}
+
 // ------------------------------------------------------- bulk async copies
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src 16-byte aligned, bytes a multiple of 16.
@@ -113,20 +125,18 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 
 // ------------------------------------------------------------ INT4 decode
 // A packed word holds 8 offset-binary nibbles u = q + 8.  Nibble positions
-// j and j+4 form register j of an m16n8k16 A fragment: (128 + u) is built by
-// OR-ing the nibble into the mantissa of BF16 128.0, then 136 is subtracted,
-// leaving q exactly.
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&a)[4]) {
-  const uint32_t kMagic = 0x43004300u;  // bf16x2 (128, 128)
-  const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.f, 136.f);
+// j and j+4 form register j of an m16n8k16 A fragment.  OR-ing a nibble into
+// the mantissa of BF16 128.0 gives the exact value 128 + u = q + 136; the
+// constant 136 is removed after the MMA (136 * sum of the activations).
+// `mask` (0x000F000F) and `magic` (0x43004300, bf16x2 (128, 128)) are passed
+// in registers so that each register costs one 3-input LOP3.
+__device__ __forceinline__ void decode_word_offset136(uint32_t w, uint32_t mask, uint32_t magic,
+                                                      uint32_t (&a)[4]) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | kMagic;
-    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
-    h = __hsub2(h, k136);
-    a[j] = *reinterpret_cast<uint32_t*>(&h);
-  }
+  for (int j = 0; j < 4; ++j)
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[j]) : "r"(w >> (4 * j)), "r"(mask), "r"(magic));
 }
+constexpr uint32_t kBf16x2Neg136 = 0xC308C308u;  // bf16x2 (-136, -136)
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }

@@ -3,27 +3,32 @@
 // [Humming] "워크로드별 튜닝 및 JIT 컴파일": at small batch a multistage
 // async-copy + MMA pipeline beats TMA + UMMA; [Chord] "인덱스 커널 기법":
 // decode is a weight-streaming problem.  Design on sm_103a:
-//   * grid (weight tile, local expert); a CTA streams one expert's 128-row
-//     weight tile over all of K once per pass of up to NT*8 of the expert's
-//     rows, so each weight byte is read once per expert (not once per block);
+//   * grid (64-row weight tile, local expert); a CTA streams one expert's tile
+//     over all of K once per pass of up to NT*8 of the expert's rows, so each
+//     weight byte is read once per expert, not once per row block;
 //   * one producer warp issues 1-D bulk async copies (TMA engine) of the
 //     contiguous packed units and of the expert's activation rows into a
-//     STAGES-deep ring, completing on mbarriers;
-//   * four consumer warps each own 32 weight rows (two 16-row slabs),
-//     decode INT4 nibbles straight into m16n8k16 A fragments (the packed
-//     order is the fragment order), take B fragments with ldmatrix, and run
-//     mma.sync with weights as the M side and tokens as N ("swap AB");
-//   * scales are applied in FP32 per 32-wide group to a per-group partial
-//     sum, so the dequantised weights q*s are never rounded;
-//   * epilogue: SiLU(gate) * up (gate/up blobs pair the two slabs of a warp)
-//     or a plain store, BF16, rows in sorted order.
+//     STAGES-deep shared-memory ring, completing on mbarriers;
+//   * four consumer warps, one 16-row slab each, decode INT4 nibbles straight
+//     into m16n8k16 A fragments (the packed order is the fragment order),
+//     take B fragments with ldmatrix, and run mma.sync with weights as the M
+//     side and tokens as N ("swap AB");
+//   * decoding is one shift and one LOP3 per register: the MMA sees q + 136
+//     (exact in BF16); per 32-wide scale group the accumulator chain is
+//     seeded with -136 * (sum of the group's activations), itself one MMA of
+//     a constant -136 fragment, so the chain yields sum(q * x) exactly as a
+//     dot product of exact products; the group's scale is then applied in
+//     FP32 (no rounding of q * s);
+//   * epilogue: SiLU(gate) * up (a gate/up slab holds gate rows g and up rows
+//     g + 8 of the same intermediate index, so both land in one thread) or a
+//     plain store, BF16, rows in sorted order.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace chord {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = kSlabs;                     // one slab per warp
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kUnitsPerStage = 4;                          // 256 of K per stage
 constexpr int kXRowBytes = kUnitsPerStage * kUnitK * 2;    // 512
@@ -47,6 +52,8 @@ struct SmallArgs {
   int N, K, topk, ldc, n_tiles, E_local;
   int64_t tile_bytes;
   uint32_t need_flags;
+  // decode constants, passed at run time so they stay in registers
+  uint32_t nib_mask, nib_magic, neg136;
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -71,8 +78,44 @@ __device__ bool header_ok(const SmallArgs& a) {
          (h->flags & a.need_flags) == a.need_flags;
 }
 
+// One 64-wide K unit for one warp's slab and NT token tiles: per 32-wide
+// group, the chain  -136*sum(x) [2 MMAs]  +  (q+136)*x [2 MMAs]  = sum(q*x),
+// then acc += scale * chain in FP32.  Every token tile is computed (columns
+// of unused tokens are discarded by the epilogue), so no MMA is predicated.
+template <int NT>
+__device__ __forceinline__ void unit_mma(uint32_t ub, uint32_t xu, uint32_t q_off, uint32_t s_off,
+                                         const uint32_t (&neg136)[4], uint32_t mask,
+                                         uint32_t magic, float (&acc)[NT][4]) {
+  const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint4 q = lds128(ub + q_off);
+  const uint2 sc = lds64(ub + s_off);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t bf[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) ldmatrix_x4(bf[n], xu + n * 8 * kXPitch + half * 64);
+    uint32_t a0[4], a1[4];
+    decode_word_offset136(half ? q.z : q.x, mask, magic, a0);
+    decode_word_offset136(half ? q.w : q.y, mask, magic, a1);
+    const uint32_t sw = half ? sc.y : sc.x;
+    const float s_lo = bf16lo_to_f32(sw), s_hi = bf16hi_to_f32(sw);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      float c[4];
+      mma_bf16_16816(c, neg136, bf[n][0], bf[n][1], zero4);  // -136 * sum x, k 0..15
+      mma_bf16_16816(c, neg136, bf[n][2], bf[n][3], c);      //            k 16..31
+      mma_bf16_16816(c, a0, bf[n][0], bf[n][1], c);          // + (q+136) x
+      mma_bf16_16816(c, a1, bf[n][2], bf[n][3], c);
+      acc[n][0] = fmaf(s_lo, c[0], acc[n][0]);
+      acc[n][1] = fmaf(s_lo, c[1], acc[n][1]);
+      acc[n][2] = fmaf(s_hi, c[2], acc[n][2]);
+      acc[n][3] = fmaf(s_hi, c[3], acc[n][3]);
+    }
+  }
+}
+
 template <int NT, int STAGES, bool GATHER, int EPI>
-__global__ void __launch_bounds__(kThreads) gemm_small_kernel(SmallArgs a) {
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gemm_small_kernel(SmallArgs a) {
   using Cfg = SmallCfg<NT>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -109,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) gemm_small_kernel(SmallArgs a) {
     bool ok = true;
     for (int it = 0; it < iters && ok; ++it) {
       const int s = it % STAGES;
-      if (it >= STAGES) ok = mbar_wait(&empty_bar[s], ((it / STAGES) - 1) & 1, a.status);
+      if (it >= STAGES) ok = mbar_wait_backoff(&empty_bar[s], ((it / STAGES) - 1) & 1, a.status);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       const int pass = it / k_stages, ks = it - pass * k_stages;
@@ -142,103 +185,57 @@ __global__ void __launch_bounds__(kThreads) gemm_small_kernel(SmallArgs a) {
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, t = lane & 3;
   const uint32_t smem_base = smem_u32(smem);
-  const int slab0 = 2 * warp;
+  const uint32_t q_off = warp * 512 + lane * 16;             // this warp's slab, this lane
+  const uint32_t s_off = kUnitQBytes + warp * 64 + g * 8;
+  const uint32_t x_off = Cfg::kWBytes + (lane & 7) * kXPitch + (lane >> 3) * 16;
+  const uint32_t neg136[4] = {a.neg136, a.neg136, a.neg136, a.neg136};
+  const uint32_t mask = a.nib_mask, magic = a.nib_magic;
   for (int pass = 0; pass < passes; ++pass) {
     const int rows = min(Cfg::kRowsPerPass, cnt - pass * Cfg::kRowsPerPass);
-    const int active = (rows + 7) >> 3;
-    float acc[2][NT][4];
+    float acc[NT][4];
 #pragma unroll
-    for (int sl = 0; sl < 2; ++sl)
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[sl][n][i] = 0.f;
+      for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
 
     for (int ks = 0; ks < k_stages; ++ks) {
       const int it = pass * k_stages + ks;
       const int s = it % STAGES;
       if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status)) return;
-      const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
       const uint32_t st = smem_base + s * Cfg::kStageBytes;
-      const uint32_t xs = st + Cfg::kWBytes + (lane & 7) * kXPitch + (lane >> 3) * 16;
+      const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
+      if (units == kUnitsPerStage) {
 #pragma unroll
-      for (int u = 0; u < kUnitsPerStage; ++u) {
-        if (u >= units) break;
-        const uint32_t ub = st + u * kUnitBytes;
-        const uint4 q0 = lds128(ub + slab0 * 512 + lane * 16);
-        const uint4 q1 = lds128(ub + (slab0 + 1) * 512 + lane * 16);
-        const uint2 s0 = lds64(ub + kUnitQBytes + slab0 * 64 + g * 8);
-        const uint2 s1 = lds64(ub + kUnitQBytes + (slab0 + 1) * 64 + g * 8);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t bf[NT][4];
-#pragma unroll
-          for (int n = 0; n < NT; ++n)
-            if (n < active) ldmatrix_x4(bf[n], xs + n * 8 * kXPitch + (u * kUnitK + half * 32) * 2);
-          float tmp[2][NT][4];
-#pragma unroll
-          for (int sl = 0; sl < 2; ++sl)
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) tmp[sl][n][i] = 0.f;
-#pragma unroll
-          for (int stp = 0; stp < 2; ++stp) {
-            const int j = half * 2 + stp;
-            const uint32_t w0 = j == 0 ? q0.x : j == 1 ? q0.y : j == 2 ? q0.z : q0.w;
-            const uint32_t w1 = j == 0 ? q1.x : j == 1 ? q1.y : j == 2 ? q1.z : q1.w;
-            uint32_t a0[4], a1[4];
-            dequant_word(w0, a0);
-            dequant_word(w1, a1);
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-              if (n < active) {
-                mma_bf16_16816(tmp[0][n], a0, bf[n][2 * stp], bf[n][2 * stp + 1], tmp[0][n]);
-                mma_bf16_16816(tmp[1][n], a1, bf[n][2 * stp], bf[n][2 * stp + 1], tmp[1][n]);
-              }
-            }
-          }
-          const uint32_t sw0 = half ? s0.y : s0.x;
-          const uint32_t sw1 = half ? s1.y : s1.x;
-          const float sg0 = bf16lo_to_f32(sw0), sh0 = bf16hi_to_f32(sw0);
-          const float sg1 = bf16lo_to_f32(sw1), sh1 = bf16hi_to_f32(sw1);
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            acc[0][n][0] = fmaf(sg0, tmp[0][n][0], acc[0][n][0]);
-            acc[0][n][1] = fmaf(sg0, tmp[0][n][1], acc[0][n][1]);
-            acc[0][n][2] = fmaf(sh0, tmp[0][n][2], acc[0][n][2]);
-            acc[0][n][3] = fmaf(sh0, tmp[0][n][3], acc[0][n][3]);
-            acc[1][n][0] = fmaf(sg1, tmp[1][n][0], acc[1][n][0]);
-            acc[1][n][1] = fmaf(sg1, tmp[1][n][1], acc[1][n][1]);
-            acc[1][n][2] = fmaf(sh1, tmp[1][n][2], acc[1][n][2]);
-            acc[1][n][3] = fmaf(sh1, tmp[1][n][3], acc[1][n][3]);
-          }
-        }
+        for (int u = 0; u < kUnitsPerStage; ++u)
+          unit_mma<NT>(st + u * kUnitBytes, st + x_off + u * kUnitK * 2, q_off, s_off, neg136, mask,
+                       magic, acc);
+      } else {
+#pragma unroll 1
+        for (int u = 0; u < units; ++u)
+          unit_mma<NT>(st + u * kUnitBytes, st + x_off + u * kUnitK * 2, q_off, s_off, neg136, mask,
+                       magic, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
 
     // ------------------------------------------------------------ epilogue
-    const int r0 = off + pass * Cfg::kRowsPerPass;
+    const size_t r0 = static_cast<size_t>(off) + pass * Cfg::kRowsPerPass;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int tok = n * 8 + 2 * t + (i & 1);
+      for (int i = 0; i < 2; ++i) {
+        const int tok = n * 8 + 2 * t + i;
         if (tok >= rows) continue;
-        const size_t r = static_cast<size_t>(r0 + tok);
-        const int rr = g + 8 * (i >> 1);
+        uint16_t* crow = a.C + (r0 + tok) * a.ldc;
         if (EPI == CHORD_EPI_SILU_MUL) {
-          const int col = 64 * nt + 16 * warp + rr;
-          const float h = silu_f32(acc[0][n][i]) * acc[1][n][i];
-          a.C[r * a.ldc + col] = f32_to_bf16_rn(h);
+          // acc[n][i]: gate of index i0 + g; acc[n][2 + i]: up of the same index
+          const int col = 32 * nt + 8 * warp + g;
+          crow[col] = f32_to_bf16_rn(silu_f32(acc[n][i]) * acc[n][2 + i]);
         } else {
-#pragma unroll
-          for (int sl = 0; sl < 2; ++sl) {
-            const int col = kTileRows * nt + 32 * warp + 16 * sl + rr;
-            if (col < a.N) a.C[r * a.ldc + col] = f32_to_bf16_rn(acc[sl][n][i]);
-          }
+          const int col = kTileRows * nt + 16 * warp + g;
+          if (col < a.N) crow[col] = f32_to_bf16_rn(acc[n][i]);
+          if (col + 8 < a.N) crow[col + 8] = f32_to_bf16_rn(acc[n][2 + i]);
         }
       }
     }
@@ -247,12 +244,11 @@ __global__ void __launch_bounds__(kThreads) gemm_small_kernel(SmallArgs a) {
 
 template <int NT, int STAGES, bool GATHER, int EPI>
 cudaError_t launch_small(const SmallArgs& a, cudaStream_t st) {
-  auto kern = gemm_small_kernel<NT, STAGES, GATHER, EPI>;
   const int smem = STAGES * SmallCfg<NT>::kStageBytes;
   cudaError_t err = ensure_smem_limit<gemm_small_kernel<NT, STAGES, GATHER, EPI>>(smem);
   if (err != cudaSuccess) return err;
   dim3 grid(a.n_tiles, a.E_local);
-  kern<<<grid, kThreads, smem, st>>>(a);
+  gemm_small_kernel<NT, STAGES, GATHER, EPI><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -286,9 +282,13 @@ cudaError_t gemm_small_launch(const GemmLaunch& g, int rows_per_pass, cudaStream
   a.tile_bytes = h.tile_bytes;
   a.need_flags = g.epilogue == CHORD_EPI_SILU_MUL ? kPackFlagGateUp : 0u;
   a.ldc = g.epilogue == CHORD_EPI_SILU_MUL ? g.N / 2 : g.N;
+  a.nib_mask = 0x000F000Fu;
+  a.nib_magic = 0x43004300u;
+  a.neg136 = kBf16x2Neg136;
+  // 4 stages: 53.8 KB (NT=1, 4 CTAs/SM), 70.7 KB (NT=2, 3 CTAs/SM), 104 KB (NT=4, 2 CTAs/SM)
   if (rows_per_pass <= 8) return dispatch_mode<1, 4>(a, g.gather, g.epilogue, st);
   if (rows_per_pass <= 16) return dispatch_mode<2, 4>(a, g.gather, g.epilogue, st);
-  return dispatch_mode<4, 6>(a, g.gather, g.epilogue, st);
+  return dispatch_mode<4, 4>(a, g.gather, g.epilogue, st);
 }
 
 }  // namespace chord

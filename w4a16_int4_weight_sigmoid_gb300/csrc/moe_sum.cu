@@ -21,16 +21,33 @@ __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* __res
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int j = 0; j < topk; ++j) {
-    const int p = __ldg(pos + static_cast<size_t>(t) * topk + j);
-    if (p < 0) continue;
-    const float wj = __ldg(w + static_cast<size_t>(t) * topk + j);
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(p) * H + c));
-    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+  // Slots in groups of 8: positions and weights first, then every row load of
+  // the group, so the loads overlap instead of forming a dependent chain.
+  for (int j0 = 0; j0 < topk; j0 += 8) {
+    int p[8];
+    float wj[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = fmaf(wj, bf16lo_to_f32(vv[i]), acc[2 * i]);
-      acc[2 * i + 1] = fmaf(wj, bf16hi_to_f32(vv[i]), acc[2 * i + 1]);
+    for (int j = 0; j < 8; ++j) {
+      const bool in = j0 + j < topk;
+      const size_t o = static_cast<size_t>(t) * topk + (in ? j0 + j : 0);
+      p[j] = in ? __ldg(pos + o) : -1;
+      wj[j] = in ? __ldg(w + o) : 0.f;
+    }
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = make_uint4(0, 0, 0, 0);
+      if (p[j] >= 0) v[j] = __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(p[j]) * H + c));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (p[j] < 0) continue;
+      const uint32_t vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(wj[j], bf16lo_to_f32(vv[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wj[j], bf16hi_to_f32(vv[i]), acc[2 * i + 1]);
+      }
     }
   }
   uint32_t o[4];

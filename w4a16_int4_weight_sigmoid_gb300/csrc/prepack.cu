@@ -6,19 +6,21 @@
 //
 //   header (256 B) | expert 0: tile 0: unit 0 | unit 1 | ... | tile 1 ... | expert 1 ...
 //
-// A tile is 128 weight rows ("physical rows") over all of K; a unit is the
-// tile's 64-wide K slice, 4608 bytes:
-//   q part, 4096 B: [slab 0..7][lane 0..31][4 words]; slab = 16 rows; word j
-//     (k16 step j of the unit) holds the lane's m16n8k16 A-fragment as 8
-//     offset-binary nibbles u = q + 8: nibble p (p & 3 = pp, p >> 2 = hi) is
-//     row g + 8*(pp & 1), column 2t + 8*(pp >> 1) + hi of the 16x16 block,
+// A tile is 64 weight rows ("physical rows", 4 slabs of 16) over all of K; a
+// unit is the tile's 64-wide K slice, 2304 bytes, contiguous so one bulk copy
+// moves any run of units:
+//   q part, 2048 B: [slab 0..3][lane 0..31][4 words]; word j (k16 step j of
+//     the unit) holds the lane's m16n8k16 A fragment as 8 offset-binary
+//     nibbles u = q + 8: nibble p (p & 3 = pp, p >> 2 = hi) is row
+//     g + 8*(pp & 1), column 2t + 8*(pp >> 1) + hi of the 16x16 block,
 //     with g = lane / 4, t = lane % 4.
-//   s part, 512 B: [slab][g 0..7][group 0..1][row half 0..1] BF16 scales of
+//   s part, 256 B: [slab][g 0..7][group 0..1][row half 0..1] BF16 scales of
 //     rows g and g+8 for the unit's two 32-wide groups.
-// Physical -> logical rows: plain weights: tile nt row p = logical 128*nt + p
-// (rows >= N are zero).  Gate/up weights (N = 2I): warp-sized 32-row blocks
-// pair 16 gate rows with the 16 up rows of the same intermediate index:
-// row p of tile nt = (p/16 % 2) * I + 64*nt + 16*(p/32) + p%16.
+// Physical -> logical rows: plain weights: tile nt row p = logical 64*nt + p
+// (rows >= N are zero).  Gate/up weights (N = 2I): slab s of tile nt holds
+// intermediate indices i = 32*nt + 8*s + (0..7), gate rows in its first 8
+// rows and the matching up rows in its last 8, so one MMA thread holds the
+// gate and up values of the same (i, token).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -28,7 +30,8 @@ namespace {
 __device__ __forceinline__ int logical_row(int nt, int p, int N, bool gate_up) {
   if (gate_up) {
     const int I = N / 2;
-    return ((p >> 4) & 1) * I + 64 * nt + 16 * (p >> 5) + (p & 15);
+    const int r = p & 15;
+    return (r >> 3) * I + 32 * nt + 8 * (p >> 4) + (r & 7);
   }
   const int n = kTileRows * nt + p;
   return n < N ? n : -1;
@@ -37,12 +40,12 @@ __device__ __forceinline__ int logical_row(int nt, int p, int N, bool gate_up) {
 __global__ void prepack_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s, int E,
                                int N, int K, int n_tiles, bool gate_up, uint8_t* __restrict__ out) {
   const int n_units = K / kUnitK;
-  const long long total = static_cast<long long>(E) * n_tiles * n_units * 8 * 32;
+  const long long total = static_cast<long long>(E) * n_tiles * n_units * kSlabs * 32;
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= total) return;
   const int lane = static_cast<int>(gid & 31);
-  const int slab = static_cast<int>((gid >> 5) & 7);
-  long long rest = gid >> 8;
+  const int slab = static_cast<int>((gid >> 5) % kSlabs);
+  long long rest = (gid >> 5) / kSlabs;
   const int kt = static_cast<int>(rest % n_units);
   rest /= n_units;
   const int nt = static_cast<int>(rest % n_tiles);
@@ -74,6 +77,7 @@ __global__ void prepack_kernel(const uint8_t* __restrict__ q, const uint16_t* __
                           ((static_cast<size_t>(e) * n_tiles + nt) * n_units + kt) * kUnitBytes;
   uint4 v = make_uint4(words[0], words[1], words[2], words[3]);
   *reinterpret_cast<uint4*>(out + unit_off + slab * 512 + lane * 16) = v;
+  static_assert(kUnitQBytes == kSlabs * 512, "q part is 512 B per slab");
   if (t == 0) {
     const int ng = K / kGroup;
     const uint16_t* se = s + static_cast<size_t>(e) * N * ng;
@@ -126,7 +130,7 @@ cudaError_t prepack_launch(const uint8_t* q, const uint16_t* s, int E, int N, in
   prepack_header_kernel<<<1, 64, 0, st>>>(h, out);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const long long total = static_cast<long long>(E) * h.n_tiles * (K / kUnitK) * 256;
+  const long long total = static_cast<long long>(E) * h.n_tiles * (K / kUnitK) * kSlabs * 32;
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;

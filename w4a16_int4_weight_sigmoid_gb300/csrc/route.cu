@@ -38,9 +38,14 @@ __device__ __forceinline__ float sigmoid_spec(float x) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
 }
 
-// (key, id) order: larger key first; equal keys -> smaller id first.
-__device__ __forceinline__ bool better(float ka, int ia, float kb, int ib) {
-  return ka > kb || (ka == kb && ia < ib);
+// (key, id) as one integer whose order is the selection order: the key's
+// bits mapped to an order-preserving unsigned (keys are never -0.0: s > 0 and
+// s + b rounds x + (-x) to +0), then the complement of the id, so among equal
+// keys the smaller id compares larger.
+__device__ __forceinline__ uint64_t pack_key(float key, int id) {
+  const uint32_t b = __float_as_uint(key);
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<uint64_t>(ord) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(id));
 }
 
 template <int EPL>
@@ -52,49 +57,48 @@ __global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ lo
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= M) return;
   const float* row = logits + static_cast<size_t>(t) * E;
-  float key[EPL], sc[EPL];
+  // All loads first (clamped in-range addresses, no branches), so they are in
+  // flight together instead of one round trip per expert.
+  float lg[EPL], bs[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = min(lane + 32 * i, E - 1);
+    lg[i] = __ldg(row + e);
+    bs[i] = __ldg(bias + e);
+  }
+  uint64_t cand[EPL];
+  float sc[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    if (e < E) {
-      sc[i] = sigmoid_spec(__ldg(row + e));
-      key[i] = __fadd_rn(sc[i], __ldg(bias + e));
-    } else {
-      sc[i] = 0.f;
-      key[i] = -FLT_MAX;
-    }
+    sc[i] = sigmoid_spec(lg[i]);
+    cand[i] = e < E ? pack_key(__fadd_rn(sc[i], bs[i]), e) : 0;  // 0: below every candidate
   }
-  uint32_t taken = 0;
   int my_id = 0;
   float my_s = 0.f;
   for (int r = 0; r < topk; ++r) {
-    float bk = -INFINITY;
-    int bi = INT32_MAX;
-    float bs = 0.f;
+    uint64_t best = cand[0];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && better(key[i], e, bk, bi)) {
-        bk = key[i];
-        bi = e;
-        bs = sc[i];
-      }
-    }
+    for (int i = 1; i < EPL; ++i) best = cand[i] > best ? cand[i] : best;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-      if (better(ok, oi, bk, bi)) {
-        bk = ok;
-        bi = oi;
-        bs = os;
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o > best ? o : best;
+    }
+    const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+    const int owner = id & 31, slot = id >> 5;
+    float s_mine = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      if (i == slot) {
+        s_mine = sc[i];
+        if (lane == owner) cand[i] = 0;
       }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const float s_win = __shfl_sync(0xffffffffu, s_mine, owner);
     if (lane == r) {
-      my_id = bi;
-      my_s = bs;
+      my_id = id;
+      my_s = s_win;
     }
   }
   // S = s_0 + s_1 + ... in rank order, binary32.
