@@ -44,10 +44,11 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 KERNEL_SOURCES = {
-    "gate_up": ["w4a16_int4_weight_sigmoid_gb300/csrc/gemm_small.cu",
-                "w4a16_int4_weight_sigmoid_gb300/csrc/common.cuh"],
-    "down": ["w4a16_int4_weight_sigmoid_gb300/csrc/gemm_small.cu",
-             "w4a16_int4_weight_sigmoid_gb300/csrc/common.cuh"],
+    "small": ["w4a16_int4_weight_sigmoid_gb300/csrc/gemm_small.cu",
+              "w4a16_int4_weight_sigmoid_gb300/csrc/common.cuh"],
+    "large": ["w4a16_int4_weight_sigmoid_gb300/csrc/gemm_large.cu",
+              "w4a16_int4_weight_sigmoid_gb300/csrc/tc5.cuh",
+              "w4a16_int4_weight_sigmoid_gb300/csrc/common.cuh"],
 }
 
 
@@ -110,17 +111,17 @@ def source_sha(files):
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel: str, workload: str):
+def committed_traffic(kernel: str, workload: str, gemm_path: str):
     """DRAM bytes per launch from the committed ncu summary, if the kernel's
     sources are unchanged since the capture; else None."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    record = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(record):
         return None
-    with open(path) as f:
+    with open(record) as f:
         entries = json.load(f)
     for e in entries:
-        if e.get("kernel") == kernel and e.get("workload") == workload:
-            if e.get("source_sha") == source_sha(KERNEL_SOURCES[kernel]):
+        if e.get("kernel") == kernel and e.get("workload") == workload and e.get("path", "small") == gemm_path:
+            if e.get("source_sha") == source_sha(KERNEL_SOURCES[gemm_path]):
                 return e.get("dram_bytes_per_launch")
     return None
 
@@ -197,7 +198,9 @@ class Replica:
         self.logits_pinned = torch.from_numpy(d["logits"]).pin_memory()
         del d
         M, k, E, H, I = shape.M, shape.topk, shape.E_local, shape.H, shape.I
-        self.bm = 16
+        self.plan = chord.chord_moe_layer_plan(M, shape.E_total, k)
+        self.large = self.plan.path == chord.CHORD_PATH_LARGE_M
+        self.bm = 16 if self.large else self.plan.rows_per_pass   # the layer's own choice
         self.cap = chord.chord_moe_align_capacity(M, k, E, self.bm)
         i32, dev = torch.int32, device
         self.tw = torch.empty((M, k), dtype=torch.float32, device=dev)
@@ -214,8 +217,12 @@ class Replica:
         self.y = torch.empty((self.cap, H), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros(1, dtype=i32, device=dev)
-        self.plan = chord.chord_moe_layer_plan(M, shape.E_total, k)
+        self.ws_gu = torch.zeros(chord.chord_w4a16_moe_gemm_workspace_bytes(self.cap, H, True),
+                                 dtype=torch.uint8, device=dev)
+        self.ws_dn = torch.zeros(chord.chord_w4a16_moe_gemm_workspace_bytes(self.cap, I, False),
+                                 dtype=torch.uint8, device=dev)
         self.align_launches = 1 if wsb == 0 else 2
+        self.gemm_launches = 3 if self.large else 2     # + the row gather on the tcgen05 path
 
     # the layer's steps, each one C-ABI call (the calls chord_moe_layer makes)
     def route_align(self):
@@ -229,15 +236,17 @@ class Replica:
         from w4a16_int4_weight_sigmoid_gb300 import chord
         s = self.shape
         chord.chord_w4a16_moe_gemm(self.x, True, self.layer.w13, s.E_local, 2 * s.I, s.H, s.M, s.topk,
-                                   self.sorted, self.counts, self.offsets, chord.CHORD_EPI_SILU_MUL,
-                                   self.h, tuning=self.plan, dev_status=self.status)
+                                   self.sorted, self.eids, self.ntpp, self.counts, self.offsets, self.bm,
+                                   chord.CHORD_EPI_SILU_MUL, self.h, self.ws_gu, tuning=self.plan,
+                                   dev_status=self.status)
 
     def down(self):
         from w4a16_int4_weight_sigmoid_gb300 import chord
         s = self.shape
         chord.chord_w4a16_moe_gemm(self.h, False, self.layer.w2, s.E_local, s.H, s.I, s.M, s.topk,
-                                   self.sorted, self.counts, self.offsets, chord.CHORD_EPI_STORE,
-                                   self.y, tuning=self.plan, dev_status=self.status)
+                                   self.sorted, self.eids, self.ntpp, self.counts, self.offsets, self.bm,
+                                   chord.CHORD_EPI_STORE, self.y, self.ws_dn, tuning=self.plan,
+                                   dev_status=self.status)
 
     def combine(self):
         from w4a16_int4_weight_sigmoid_gb300 import chord
@@ -364,8 +373,8 @@ def run_ours(args, world, rank, local):
         ach = alg[dom]["flops"] / t_s / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = committed_traffic(dom, shape.name)
-    roof["kernel"] = f"gemm_small ({dom})"
+    roof["traffic"] = committed_traffic(dom, shape.name, "large" if reps[0].large else "small")
+    roof["kernel"] = f"{'gemm_large (tcgen05)' if reps[0].large else 'gemm_small'} ({dom})"
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     roof["algorithmic_bytes_per_launch"] = alg[dom]["bytes"]
     roof["algorithmic_flops_per_launch"] = alg[dom]["flops"]
@@ -404,7 +413,7 @@ def run_ours(args, world, rank, local):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
            "api": "chord_moe_layer"}
 
-    launches_per_step = reps[0].align_launches + 4
+    launches_per_step = reps[0].align_launches + reps[0].gemm_launches + 2   # + route, combine
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",

@@ -185,23 +185,37 @@ int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E,
                         int group, int gate_up, void* packed, size_t packed_bytes, void* stream);
 
 /* ------------------------------------------------------- grouped W4A16 GEMM
- * Indexed MoE GEMM ([Chord] "핵심 기여", "인덱스 커널 기법"): for every
- * local expert e and row r in expert_offsets[e] .. + expert_counts[e]:
+ * Indexed MoE GEMM ([Chord] "핵심 기여", "인덱스 커널 기법") over the align
+ * buffers ([Router] "코드 분석": sorted_token_ids, expert_ids,
+ * num_tokens_post_padded; expert counts and offsets): for every row r of a
+ * block b < num_tokens_post_padded / block_m with expert e = expert_ids[b]
+ * and r < expert_offsets[e] + expert_counts[e]:
  *   acc[r, n] = sum_k A[row(r), k] * q[e, n, k] * s[e, n, k/32]   (FP32 accumulate)
  * with row(r) = sorted_token_ids[r] / topk when a_gather = 1 (A = the
  * token activations [M, K]) and row(r) = r when a_gather = 0 (A = rows in
  * sorted order [capacity, K], e.g. the gate/up output).
+ *   block_m  the BLOCK_M the align buffers were built with
  *   C        BF16 [capacity, N] (STORE) or [capacity, N/2] (SILU_MUL); padding
  *            rows are not written
+ *   workspace  chord_w4a16_moe_gemm_workspace_bytes() bytes, 16-byte aligned.
+ *            Its first 256 bytes are work-queue counters: zero them once when
+ *            the workspace is allocated; every call leaves them zero (a call
+ *            that stops on a device timeout may not).  With a_gather = 1 the
+ *            tensor-core path also stages the gathered rows there.
  *   dev_status  device int for errors found on the device (may be NULL)
- * The expert offsets/counts are read on the device, so the call never waits
- * for the host (graph-safe).
+ * Two paths ([Humming] "워크로드별 튜닝 및 JIT 컴파일": async-copy + MMA at
+ * small batch, TMA + UMMA at large batch), chosen from the expected rows per
+ * expert M*topk/E_local unless tuning->path says otherwise: a weight-
+ * streaming register-MMA path, and a tcgen05/TMEM path (needs N % 128 == 0).
+ * Everything is read on the device, so the call never waits for the host.
  */
+size_t chord_w4a16_moe_gemm_workspace_bytes(size_t capacity, int K, int a_gather);
 int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w, int E_local,
                          int N, int K, int M, int topk, const int32_t* sorted_token_ids,
-                         const int32_t* expert_counts, const int32_t* expert_offsets,
+                         const int32_t* expert_ids, const int32_t* num_tokens_post_padded,
+                         const int32_t* expert_counts, const int32_t* expert_offsets, int block_m,
                          size_t capacity, int epilogue, chord_bf16* C, const chord_tuning* tuning,
-                         int* dev_status, void* stream);
+                         void* workspace, size_t ws_bytes, int* dev_status, void* stream);
 
 /* --------------------------------------------------------- top-k weighted sum
  * moe_fused_mul_sum ([HumPR] "왜 이게 좋은가" 3: weight multiply and sum):

@@ -13,9 +13,11 @@ from gpu_util import assert_close_to_oracle, bf16_to_np, ensure_lib, to_device
 
 pytestmark = pytest.mark.gpu
 
-# GEMM alone: FP32 accumulation of exact products, one BF16 rounding of C.
-GEMM_MAXABS = 8e-3
-GEMM_FROB = 3e-3
+# GEMM alone.  Register-MMA path: FP32 accumulation of exact products, one
+# BF16 rounding of C.  Tensor-core path: the dequantised weight q*s is also
+# rounded once to BF16 (up to 2^-9 relative for |q| in 3, 5, 6, 7), which
+# roughly doubles the RMS error, so it is held to the layer's parity bar.
+GEMM_TOL = {chord.CHORD_PATH_SMALL_M: (8e-3, 3e-3), chord.CHORD_PATH_LARGE_M: (1e-2, 5e-3)}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -23,22 +25,37 @@ def _lib():
     ensure_lib()
 
 
-def _problem(M, K, N, E_total, E_local, begin, topk, seed, zipf=0.0):
+def _problem(M, K, N, E_total, E_local, begin, topk, seed, bm=16, zipf=0.0):
     logits, bias = wl.router_inputs(M, E_total, seed, zipf)
     _, ids, _ = oracle.route(logits, bias, topk)
-    al = oracle.moe_align(ids, begin, E_local, 16)
+    al = oracle.moe_align(ids, begin, E_local, bm)
     x = wl.activations(M, K, seed)
     q = wl.int4_weights(E_local, N, K, seed, wl.S_Q13)
     s = wl.group_scales(E_local, N, K, seed, wl.S_S13)
     return ids, al, x, q, s
 
 
-def _upload_align(al, M, topk, E_local):
-    cap = max(oracle.align_capacity(M, topk, E_local, 16), 16)
+def _upload_align(al, M, topk, E_local, bm):
+    cap = max(oracle.align_capacity(M, topk, E_local, bm), bm)
+    n = al["num_tokens_post_padded"]
     st = np.full(cap, M * topk, np.int32)
-    st[:al["num_tokens_post_padded"]] = al["sorted_token_ids"]
-    return (cap, torch.from_numpy(st).cuda(), torch.from_numpy(al["expert_counts"]).cuda(),
-            torch.from_numpy(al["expert_offsets"]).cuda())
+    st[:n] = al["sorted_token_ids"]
+    eids = np.full(cap // bm, -1, np.int32)
+    eids[:n // bm] = al["expert_ids"]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+    return (cap, t(st), t(eids), t(np.array([n])), t(al["expert_counts"]),
+            t(al["expert_offsets"]))
+
+
+def _run_gemm(A, gather, packed, E_local, N, K, M, topk, up, bm, epi, C, path, status):
+    cap, st, eids, ntpp, cnt, off = up
+    ws = torch.zeros(chord.chord_w4a16_moe_gemm_workspace_bytes(cap, K, gather), dtype=torch.uint8,
+                     device="cuda")
+    tun = chord.chord_tuning(path, 0, 0, 0)
+    chord.chord_w4a16_moe_gemm(A, gather, packed, E_local, N, K, M, topk, st, eids, ntpp, cnt, off, bm,
+                               epi, C, ws, tuning=tun, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(ws[:8].view(torch.int32).abs().sum().item()) == 0, "work counters must be left at zero"
 
 
 def _oracle_rows(A_rows_bf16, q, s, al, topk, epi, gather):
@@ -56,57 +73,65 @@ def _oracle_rows(A_rows_bf16, q, s, al, topk, epi, gather):
     return out
 
 
-@pytest.mark.parametrize("M,K,N,E_total,E_local,begin,topk,epi,path_rows", [
-    (40, 320, 384, 8, 8, 0, 2, chord.CHORD_EPI_STORE, None),        # 3 tiles, ragged K stage
-    (40, 320, 384, 8, 8, 0, 2, chord.CHORD_EPI_SILU_MUL, None),
-    (64, 7168, 256, 384, 48, 0, 8, chord.CHORD_EPI_SILU_MUL, None),  # Kimi K, decode rows
-    (300, 256, 144, 6, 3, 2, 2, chord.CHORD_EPI_STORE, None),       # N padded to a tile, many passes
-    (300, 512, 256, 6, 6, 0, 3, chord.CHORD_EPI_SILU_MUL, None),    # >32 rows per expert
-    (2, 128, 128, 4, 4, 0, 1, chord.CHORD_EPI_STORE, None),
-])
-def test_gemm_gather(M, K, N, E_total, E_local, begin, topk, epi, path_rows):
-    ids, al, x, q, s = _problem(M, K, N, E_total, E_local, begin, topk, 7)
-    cap, st, cnt, off = _upload_align(al, M, topk, E_local)
-    packed = prepack(to_device(q), to_device(s), epi == chord.CHORD_EPI_SILU_MUL)
-    width = N // 2 if epi == chord.CHORD_EPI_SILU_MUL else N
-    C = torch.full((cap, width), float("nan"), dtype=torch.bfloat16, device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    chord.chord_w4a16_moe_gemm(to_device(x), True, packed, E_local, N, K, M, topk, st, cnt, off, epi,
-                               C, dev_status=status)
-    torch.cuda.synchronize()
-    assert status.item() == 0
-    Cn = bf16_to_np(C)
-    for e, (rows, ref) in _oracle_rows(x, q, s, al, topk, epi, True).items():
-        assert_close_to_oracle(Cn[rows], ref, f"expert {e}", GEMM_MAXABS, GEMM_FROB)
+SMALL, LARGE = chord.CHORD_PATH_SMALL_M, chord.CHORD_PATH_LARGE_M
+STORE, SILU = chord.CHORD_EPI_STORE, chord.CHORD_EPI_SILU_MUL
+CASES = [
+    # M, K, N, E_total, E_local, begin, topk, epilogue, block_m, paths
+    (40, 320, 384, 8, 8, 0, 2, STORE, 16, (SMALL, LARGE)),       # 3 tiles, ragged K stage
+    (40, 320, 384, 8, 8, 0, 2, SILU, 8, (SMALL, LARGE)),
+    (64, 7168, 256, 384, 48, 0, 8, SILU, 8, (SMALL, LARGE)),      # Kimi K, decode rows
+    (300, 256, 144, 6, 3, 2, 2, STORE, 32, (SMALL,)),             # N padded to a tile, many blocks
+    (300, 512, 256, 6, 6, 0, 3, SILU, 16, (SMALL, LARGE)),        # ~150 rows per expert
+    (1200, 256, 256, 4, 4, 0, 2, STORE, 16, (SMALL, LARGE)),      # ~600 rows: 3 tcgen05 passes
+    (2, 128, 128, 4, 4, 0, 1, STORE, 8, (SMALL, LARGE)),
+    (96, 1024, 128, 32, 32, 0, 6, SILU, 8, (SMALL, LARGE)),       # Zipf skew: one heavy expert
+]
 
 
-def test_gemm_direct_rows_and_header_check():
-    M, K, N, E, topk = 50, 256, 128, 4, 2
-    ids, al, _, q, s = _problem(M, K, N, E, E, 0, topk, 9)
-    cap, st, cnt, off = _upload_align(al, M, topk, E)
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "m%d_k%d_n%d_e%d_bm%d_%s" % (
+    c[0], c[1], c[2], c[4], c[8], "silu" if c[7] == SILU else "store"))
+def test_gemm_gather(case):
+    M, K, N, E_total, E_local, begin, topk, epi, bm, paths = case
+    zipf = 1.1 if M == 96 else 0.0
+    ids, al, x, q, s = _problem(M, K, N, E_total, E_local, begin, topk, 7, bm, zipf)
+    up = _upload_align(al, M, topk, E_local, bm)
+    packed = prepack(to_device(q), to_device(s), epi == SILU)
+    width = N // 2 if epi == SILU else N
+    expected = _oracle_rows(x, q, s, al, topk, epi, True)
+    for path in paths:
+        for _ in range(2):    # twice: the work queue must start from zero again
+            C = torch.full((up[0], width), float("nan"), dtype=torch.bfloat16, device="cuda")
+            status = torch.zeros(1, dtype=torch.int32, device="cuda")
+            _run_gemm(to_device(x), True, packed, E_local, N, K, M, topk, up, bm, epi, C, path, status)
+            assert status.item() == 0
+            Cn = bf16_to_np(C)
+            for e, (rows, ref) in expected.items():
+                assert_close_to_oracle(Cn[rows], ref, f"path {path} expert {e}", *GEMM_TOL[path])
+
+
+@pytest.mark.parametrize("path", [SMALL, LARGE])
+def test_gemm_direct_rows_and_header_check(path):
+    M, K, N, E, topk, bm = 50, 256, 128, 4, 2, 16
+    ids, al, _, q, s = _problem(M, K, N, E, E, 0, topk, 9, bm)
+    up = _upload_align(al, M, topk, E, bm)
+    cap = up[0]
     A = wl.activations(cap, K, 10)          # one row per sorted row
     packed = prepack(to_device(q), to_device(s), False)
     C = torch.zeros((cap, N), dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    chord.chord_w4a16_moe_gemm(to_device(A), False, packed, E, N, K, M, topk, st, cnt, off,
-                               chord.CHORD_EPI_STORE, C, dev_status=status)
-    torch.cuda.synchronize()
+    _run_gemm(to_device(A), False, packed, E, N, K, M, topk, up, bm, STORE, C, path, status)
     assert status.item() == 0
     Cn = bf16_to_np(C)
-    for e, (rows, ref) in _oracle_rows(A, q, s, al, topk, chord.CHORD_EPI_STORE, False).items():
-        assert_close_to_oracle(Cn[rows], ref, f"expert {e}", GEMM_MAXABS, GEMM_FROB)
+    for e, (rows, ref) in _oracle_rows(A, q, s, al, topk, STORE, False).items():
+        assert_close_to_oracle(Cn[rows], ref, f"expert {e}", *GEMM_TOL[path])
     # a blob packed for another K is refused on the device, without a fault
     other = prepack(to_device(wl.int4_weights(E, N, 2 * K, 1, 4)),
                     to_device(wl.group_scales(E, N, 2 * K, 1, 5)), False)
-    chord.chord_w4a16_moe_gemm(to_device(A), False, other, E, N, K, M, topk, st, cnt, off,
-                               chord.CHORD_EPI_STORE, C, dev_status=status)
-    torch.cuda.synchronize()
+    _run_gemm(to_device(A), False, other, E, N, K, M, topk, up, bm, STORE, C, path, status)
     assert status.item() == chord.CHORD_ERR_PREPACK_MISMATCH
     # a plain blob used for SiLU*mul is refused too
     status.zero_()
-    chord.chord_w4a16_moe_gemm(to_device(A), False, packed, E, N, K, M, topk, st, cnt, off,
-                               chord.CHORD_EPI_SILU_MUL, C, dev_status=status)
-    torch.cuda.synchronize()
+    _run_gemm(to_device(A), False, packed, E, N, K, M, topk, up, bm, SILU, C, path, status)
     assert status.item() == chord.CHORD_ERR_PREPACK_MISMATCH
 
 

@@ -56,8 +56,9 @@ _SIGS = {
     "chord_moe_align_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _Z, _P, _P, _P, _P, _P, _P, _P]),
     "chord_w4a16_prepack_bytes": (_Z, [_I, _I, _I, _I]),
     "chord_w4a16_prepack": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
-    "chord_w4a16_moe_gemm": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _I, _P, _P,
-                                  _P, _P]),
+    "chord_w4a16_moe_gemm_workspace_bytes": (_Z, [_Z, _I, _I]),
+    "chord_w4a16_moe_gemm": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _Z, _I,
+                                  _P, _P, _P, _Z, _P, _P]),
     "chord_moe_sum": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "chord_moe_layer_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "chord_moe_layer_plan": (_I, [_I, _I, _I, _P]),
@@ -177,17 +178,26 @@ def chord_w4a16_prepack(qweight, scales, gate_up: bool, packed, group: int = 32,
         int(gate_up), _ptr(packed, torch.uint8, "packed"), packed.numel(), _stream(stream)))
 
 
+def chord_w4a16_moe_gemm_workspace_bytes(capacity: int, K: int, a_gather: bool) -> int:
+    return lib().chord_w4a16_moe_gemm_workspace_bytes(capacity, K, int(a_gather))
+
+
 def chord_w4a16_moe_gemm(A, a_gather: bool, packed_w, E_local: int, N: int, K: int, M: int,
-                         topk: int, sorted_token_ids, expert_counts, expert_offsets, epilogue: int,
-                         C, tuning=None, dev_status=None, stream=None):
+                         topk: int, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                         expert_counts, expert_offsets, block_m: int, epilogue: int, C, workspace,
+                         tuning=None, dev_status=None, stream=None):
+    """workspace: uint8 tensor of chord_w4a16_moe_gemm_workspace_bytes() bytes whose first
+    256 bytes were zeroed once (the library keeps them zero)."""
     tun = _tuning(tuning)
     _check(lib().chord_w4a16_moe_gemm(
         _ptr(A, None, "A"), int(a_gather), _ptr(packed_w, torch.uint8, "packed_w"), E_local, N, K, M,
         topk, _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
+        _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(num_tokens_post_padded, torch.int32, "num_tokens_post_padded"),
         _ptr(expert_counts, torch.int32, "expert_counts"),
-        _ptr(expert_offsets, torch.int32, "expert_offsets"), sorted_token_ids.numel(), epilogue,
-        _ptr(C, None, "C"), tun[0] if tun else None, _ptr(dev_status, torch.int32, "dev_status"),
-        _stream(stream)))
+        _ptr(expert_offsets, torch.int32, "expert_offsets"), block_m, sorted_token_ids.numel(),
+        epilogue, _ptr(C, None, "C"), tun[0] if tun else None, _ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 
 def chord_moe_sum(y, topk_weights, sorted_positions, out, stream=None):

@@ -38,8 +38,6 @@ int check_tuning(const chord_tuning* t) {
     return fail(CHORD_ERR_UNSUPPORTED, "batch-invariant mode is not implemented");
   if (t->path < CHORD_PATH_AUTO || t->path > CHORD_PATH_LARGE_M)
     return fail(CHORD_ERR_INVALID_ARG, "unknown path %d", t->path);
-  if (t->path == CHORD_PATH_LARGE_M)
-    return fail(CHORD_ERR_UNSUPPORTED, "large-M path not available in this build");
   if (t->rows_per_pass != 0 && t->rows_per_pass != 8 && t->rows_per_pass != 16 && t->rows_per_pass != 32)
     return fail(CHORD_ERR_INVALID_ARG, "rows_per_pass=%d not in {0, 8, 16, 32}", t->rows_per_pass);
   return CHORD_OK;
@@ -53,17 +51,29 @@ int rows_per_pass_for(double tok_e) {
   return 32;
 }
 
-constexpr int kLayerBlockM = 16;
+// Expected rows per expert at or above which the tensor-core (tcgen05) path
+// is used; [Chord] "인덱스 커널 기법" switches schedules around 80 rows per
+// expert.
+constexpr double kLargeTokE = 64.0;
+constexpr size_t kWorkBytes = 256;   // work-queue counters at the start of a GEMM workspace
+
+// BLOCK_M the layer aligns with: one small-M pass per block, or 16 (the
+// tcgen05 path pads each expert's rows to 16 only).
+int layer_block_m(const chord_tuning& plan) {
+  return plan.path == CHORD_PATH_LARGE_M ? 16 : plan.rows_per_pass;
+}
 
 struct LayerWs {
-  size_t tw, ids, sorted, eids, ntpp, counts, offsets, pos, align_ws, h, y, total;
+  size_t work, tw, ids, sorted, eids, ntpp, counts, offsets, pos, align_ws, h, y, total;
   size_t cap;
+  int bm;
 };
 
-LayerWs layer_ws(int M, int H, int I, int E_local, int topk) {
+LayerWs layer_ws(int M, int H, int I, int E_local, int topk, int bm) {
   LayerWs w{};
   const size_t mk = static_cast<size_t>(M) * topk;
-  w.cap = chord_moe_align_capacity(M, topk, E_local, kLayerBlockM);
+  w.bm = bm;
+  w.cap = chord_moe_align_capacity(M, topk, E_local, bm);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -73,16 +83,30 @@ LayerWs layer_ws(int M, int H, int I, int E_local, int topk) {
   w.tw = take(mk * sizeof(float));
   w.ids = take(mk * sizeof(int32_t));
   w.sorted = take(w.cap * sizeof(int32_t));
-  w.eids = take(w.cap / kLayerBlockM * sizeof(int32_t));
+  w.eids = take(w.cap / bm * sizeof(int32_t));
   w.ntpp = take(sizeof(int32_t));
   w.counts = take(static_cast<size_t>(E_local) * sizeof(int32_t));
   w.offsets = take(static_cast<size_t>(E_local + 1) * sizeof(int32_t));
   w.pos = take(mk * sizeof(int32_t));
   w.align_ws = take(chord::align_workspace_bytes(static_cast<long long>(mk), E_local));
   w.h = take(w.cap * static_cast<size_t>(I) * 2);
+  // [down GEMM counters | gate/up GEMM counters | y]: the gate/up workspace is
+  // its counters followed by y's region, which holds the gathered x rows of
+  // the tcgen05 path until the down GEMM writes y.
+  w.work = take(2 * kWorkBytes);
   w.y = take(w.cap * static_cast<size_t>(H) * 2);
   w.total = o;
   return w;
+}
+
+// The largest layout over the BLOCK_M values a plan can pick.
+size_t layer_ws_max(int M, int H, int I, int E_local, int topk) {
+  size_t m = 0;
+  for (int bm : {8, 16, 32}) {
+    const size_t t = layer_ws(M, H, I, E_local, topk, bm).total;
+    m = t > m ? t : m;
+  }
+  return m;
 }
 
 int check_gemm_shapes(int N, int K, int epilogue) {
@@ -200,18 +224,28 @@ int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E,
 
 static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, int E_local, int N,
                      int K, int M, int topk, const int32_t* sorted_token_ids,
-                     const int32_t* expert_counts, const int32_t* expert_offsets, int epilogue,
-                     chord_bf16* C, const chord_tuning* tuning, double tok_e, int* dev_status,
-                     void* stream) {
+                     const int32_t* expert_ids, const int32_t* ntpp, const int32_t* expert_counts,
+                     const int32_t* expert_offsets, int block_m, size_t capacity, int epilogue,
+                     chord_bf16* C, const chord_tuning* tuning, double tok_e, void* workspace,
+                     size_t ws_bytes, int* dev_status, void* stream) {
   int rc = check_tuning(tuning);
   if (rc) return rc;
   rc = check_gemm_shapes(N, K, epilogue);
   if (rc) return rc;
   if (E_local < 1 || M < 0 || topk < 1) return fail(CHORD_ERR_INVALID_ARG, "bad E_local/M/topk");
-  if (!A || !packed_w || !C || !expert_counts || !expert_offsets || (a_gather && !sorted_token_ids))
+  if (!valid_block_m(block_m)) return fail(CHORD_ERR_INVALID_ARG, "block_m=%d not in {8,16,32,64,128}", block_m);
+  if (!A || !packed_w || !C || !expert_counts || !expert_offsets || !expert_ids || !ntpp ||
+      (a_gather && !sorted_token_ids))
     return fail(CHORD_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(A) || !aligned16(packed_w)) return fail(CHORD_ERR_INVALID_ARG, "A and packed_w must be 16-byte aligned");
+  if (!workspace || ws_bytes < kWorkBytes || !aligned16(workspace))
+    return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "GEMM workspace must hold at least %zu aligned bytes", kWorkBytes);
   if (M == 0) return CHORD_OK;
+  int path = tuning && tuning->path ? tuning->path : CHORD_PATH_AUTO;
+  if (path == CHORD_PATH_AUTO)
+    path = (tok_e >= kLargeTokE && N % 128 == 0 && E_local <= 1024) ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
+  if (path == CHORD_PATH_LARGE_M && (N % 128 != 0 || E_local > 1024))
+    return fail(CHORD_ERR_UNSUPPORTED, "tcgen05 path needs N %% 128 == 0 and E_local <= 1024");
   chord::GemmLaunch g;
   g.A = A;
   g.gather = a_gather != 0;
@@ -222,25 +256,50 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
   g.M = M;
   g.topk = topk;
   g.sorted = sorted_token_ids;
+  g.expert_ids = expert_ids;
+  g.ntpp = ntpp;
   g.counts = expert_counts;
   g.offsets = expert_offsets;
+  g.block_m = block_m;
+  g.work = static_cast<int*>(workspace);
   g.epilogue = epilogue;
   g.C = C;
   g.status = dev_status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (path == CHORD_PATH_LARGE_M) {
+    const uint16_t* B = A;
+    if (a_gather) {
+      const size_t need = kWorkBytes + capacity * static_cast<size_t>(K) * 2;
+      if (ws_bytes < need)
+        return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "GEMM workspace %zu < required %zu", ws_bytes, need);
+      uint16_t* xs = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + kWorkBytes);
+      e = chord::gather_rows_launch(A, sorted_token_ids, ntpp, topk, M * topk, K, capacity, xs, st);
+      if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+      B = xs;
+    }
+    e = chord::gemm_large_launch(g, B, capacity, st);
+    return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "tcgen05 gemm launch");
+  }
   const int rpp = tuning && tuning->rows_per_pass ? tuning->rows_per_pass : rows_per_pass_for(tok_e);
-  cudaError_t e = chord::gemm_small_launch(g, rpp, static_cast<cudaStream_t>(stream));
+  e = chord::gemm_small_launch(g, rpp, st);
   return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "gemm launch");
+}
+
+size_t chord_w4a16_moe_gemm_workspace_bytes(size_t capacity, int K, int a_gather) {
+  return kWorkBytes + (a_gather ? capacity * static_cast<size_t>(K > 0 ? K : 0) * 2 : 0);
 }
 
 int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w, int E_local,
                          int N, int K, int M, int topk, const int32_t* sorted_token_ids,
-                         const int32_t* expert_counts, const int32_t* expert_offsets,
+                         const int32_t* expert_ids, const int32_t* num_tokens_post_padded,
+                         const int32_t* expert_counts, const int32_t* expert_offsets, int block_m,
                          size_t capacity, int epilogue, chord_bf16* C, const chord_tuning* tuning,
-                         int* dev_status, void* stream) {
-  (void)capacity;
+                         void* workspace, size_t ws_bytes, int* dev_status, void* stream) {
   const double tok_e = E_local > 0 ? static_cast<double>(M) * topk / E_local : 0.0;
-  return gemm_impl(A, a_gather, packed_w, E_local, N, K, M, topk, sorted_token_ids, expert_counts,
-                   expert_offsets, epilogue, C, tuning, tok_e, dev_status, stream);
+  return gemm_impl(A, a_gather, packed_w, E_local, N, K, M, topk, sorted_token_ids, expert_ids,
+                   num_tokens_post_padded, expert_counts, expert_offsets, block_m, capacity, epilogue,
+                   C, tuning, tok_e, workspace, ws_bytes, dev_status, stream);
 }
 
 int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions,
@@ -256,7 +315,7 @@ int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t*
 int chord_moe_layer_plan(int M, int E_total, int topk, chord_tuning* plan) {
   if (!plan || M < 0 || E_total < 1 || topk < 1) return fail(CHORD_ERR_INVALID_ARG, "bad plan arguments");
   const double tok_e = static_cast<double>(M) * topk / E_total;
-  plan->path = CHORD_PATH_SMALL_M;
+  plan->path = tok_e >= kLargeTokE ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
   plan->rows_per_pass = rows_per_pass_for(tok_e);
   plan->use_f16_accum = 0;
   plan->batch_invariant = 0;
@@ -265,7 +324,7 @@ int chord_moe_layer_plan(int M, int E_total, int topk, chord_tuning* plan) {
 
 size_t chord_moe_layer_workspace_bytes(int M, int H, int I, int E_local, int topk) {
   if (M < 0 || H <= 0 || I <= 0 || E_local < 1 || topk < 1) return 0;
-  return layer_ws(M, H, I, E_local, topk).total;
+  return layer_ws_max(M, H, I, E_local, topk);
 }
 
 int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
@@ -284,8 +343,18 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
   if (M == 0) return CHORD_OK;
   if (!x || !logits || !bias || !w13_packed || !w2_packed || !out || !workspace)
     return fail(CHORD_ERR_INVALID_ARG, "null pointer");
-  const LayerWs w = layer_ws(M, H, I, E_local, topk);
-  if (ws_bytes < w.total) return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "layer workspace %zu < required %zu", ws_bytes, w.total);
+  chord_tuning plan;
+  chord_moe_layer_plan(M, E_total, topk, &plan);
+  if (tuning) {
+    if (tuning->path) plan.path = tuning->path;
+    if (tuning->rows_per_pass) plan.rows_per_pass = tuning->rows_per_pass;
+  }
+  if (plan.path == CHORD_PATH_LARGE_M && ((2 * I) % 128 != 0 || H % 128 != 0 || E_local > 1024))
+    plan.path = CHORD_PATH_SMALL_M;
+  const LayerWs w = layer_ws(M, H, I, E_local, topk, layer_block_m(plan));
+  if (ws_bytes < w.total)
+    return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "layer workspace %zu < required %zu", ws_bytes,
+                layer_ws_max(M, H, I, E_local, topk));
   if (!aligned16(workspace)) return fail(CHORD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   char* ws = static_cast<char*>(workspace);
   float* tw = topk_weights_out ? topk_weights_out : reinterpret_cast<float*>(ws + w.tw);
@@ -299,26 +368,22 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
   void* aws = ws + w.align_ws;
   chord_bf16* h = reinterpret_cast<chord_bf16*>(ws + w.h);
   chord_bf16* y = reinterpret_cast<chord_bf16*>(ws + w.y);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+  cudaError_t ce = cudaMemsetAsync(ws + w.work, 0, 2 * kWorkBytes, st);
+  if (ce != cudaSuccess) return cuda_fail(ce, "work counter reset");
   rc = chord_moe_route(logits, bias, M, E_total, topk, tw, ids, stream);
   if (rc) return rc;
-  rc = chord_moe_align(ids, M, topk, expert_begin, E_local, kLayerBlockM, w.cap, sorted, eids, ntpp,
-                       counts, offsets, pos, aws,
-                       chord_moe_align_workspace_bytes(M, topk, E_local), stream);
+  rc = chord_moe_align(ids, M, topk, expert_begin, E_local, w.bm, w.cap, sorted, eids, ntpp, counts,
+                       offsets, pos, aws, chord_moe_align_workspace_bytes(M, topk, E_local), stream);
   if (rc) return rc;
-  chord_tuning plan;
-  chord_moe_layer_plan(M, E_total, topk, &plan);
-  if (tuning) {
-    if (tuning->path) plan.path = tuning->path;
-    if (tuning->rows_per_pass) plan.rows_per_pass = tuning->rows_per_pass;
-  }
-  tuning = &plan;
   const double tok_e = static_cast<double>(M) * topk / E_total;
-  rc = gemm_impl(x, 1, w13_packed, E_local, 2 * I, H, M, topk, sorted, counts, offsets,
-                 CHORD_EPI_SILU_MUL, h, tuning, tok_e, dev_status, stream);
+  rc = gemm_impl(x, 1, w13_packed, E_local, 2 * I, H, M, topk, sorted, eids, ntpp, counts, offsets,
+                 w.bm, w.cap, CHORD_EPI_SILU_MUL, h, &plan, tok_e, ws + w.work + kWorkBytes,
+                 kWorkBytes + w.cap * static_cast<size_t>(H) * 2, dev_status, stream);
   if (rc) return rc;
-  rc = gemm_impl(h, 0, w2_packed, E_local, H, I, M, topk, sorted, counts, offsets, CHORD_EPI_STORE,
-                 y, tuning, tok_e, dev_status, stream);
+  rc = gemm_impl(h, 0, w2_packed, E_local, H, I, M, topk, sorted, eids, ntpp, counts, offsets, w.bm,
+                 w.cap, CHORD_EPI_STORE, y, &plan, tok_e, ws + w.work, kWorkBytes, dev_status, stream);
   if (rc) return rc;
   return chord_moe_sum(y, tw, pos, M, topk, H, out, stream);
 }

@@ -138,6 +138,7 @@ __device__ __forceinline__ void decode_word_offset136(uint32_t w, uint32_t mask,
 }
 constexpr uint32_t kBf16x2Neg136 = 0xC308C308u;  // bf16x2 (-136, -136)
 
+
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

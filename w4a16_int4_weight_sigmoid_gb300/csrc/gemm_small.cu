@@ -3,19 +3,24 @@
 // [Humming] "워크로드별 튜닝 및 JIT 컴파일": at small batch a multistage
 // async-copy + MMA pipeline beats TMA + UMMA; [Chord] "인덱스 커널 기법":
 // decode is a weight-streaming problem.  Design on sm_103a:
-//   * grid (64-row weight tile, local expert); a CTA streams one expert's tile
-//     over all of K once per pass of up to NT*8 of the expert's rows, so each
-//     weight byte is read once per expert, not once per row block;
+//   * persistent CTAs (as many as fit: 4 per SM for 8 rows per pass) take
+//     work items from a global counter: item = (64-row weight tile, BLOCK_M
+//     block of the aligned rows), block index fastest, read through the
+//     align buffers (expert_ids, num_tokens_post_padded); the blocks of a
+//     heavy expert become separate items that stream the same tile together
+//     (L2 hits), and the tail is one small item; the last CTA to run dry
+//     zeroes the counter;
 //   * one producer warp issues 1-D bulk async copies (TMA engine) of the
-//     contiguous packed units and of the expert's activation rows into a
-//     STAGES-deep shared-memory ring, completing on mbarriers;
+//     contiguous packed units and of the block's activation rows into a
+//     4-stage shared-memory ring, completing on mbarriers; items flow to the
+//     consumers through a small mbarrier-guarded ring;
 //   * four consumer warps, one 16-row slab each, decode INT4 nibbles straight
 //     into m16n8k16 A fragments (the packed order is the fragment order),
 //     take B fragments with ldmatrix, and run mma.sync with weights as the M
 //     side and tokens as N ("swap AB");
 //   * decoding is one shift and one LOP3 per register: the MMA sees q + 136
 //     (exact in BF16); per 32-wide scale group the accumulator chain is
-//     seeded with -136 * (sum of the group's activations), itself one MMA of
+//     seeded with -136 * (sum of the group's activations), itself two MMAs of
 //     a constant -136 fragment, so the chain yields sum(q * x) exactly as a
 //     dot product of exact products; the group's scale is then applied in
 //     FP32 (no rounding of q * s);
@@ -38,15 +43,22 @@ template <int NT>
 struct SmallCfg {
   static constexpr int kRowsPerPass = NT * 8;
   static constexpr int kWBytes = kUnitsPerStage * kUnitBytes;
-  static constexpr int kStageBytes = kWBytes + kRowsPerPass * kXPitch;
+  static constexpr int kXBytes = kRowsPerPass * kXPitch;
+  static constexpr int kStageBytes = kWBytes + kXBytes;
 };
+
+constexpr int kItemSlots = 4;
 
 struct SmallArgs {
   const uint16_t* A;
   const uint8_t* packed;
   const int32_t* sorted;
+  const int32_t* expert_ids;
+  const int32_t* ntpp;
   const int32_t* counts;
   const int32_t* offsets;
+  int* work;        // [0] next item, [1] CTAs done; zero before the launch, zero after it
+  int block_m;
   uint16_t* C;
   int* status;
   int N, K, topk, ldc, n_tiles, E_local;
@@ -78,15 +90,15 @@ __device__ bool header_ok(const SmallArgs& a) {
          (h->flags & a.need_flags) == a.need_flags;
 }
 
-// One 64-wide K unit for one warp's slab and NT token tiles: per 32-wide
-// group, the chain  -136*sum(x) [2 MMAs]  +  (q+136)*x [2 MMAs]  = sum(q*x),
-// then acc += scale * chain in FP32.  Every token tile is computed (columns
-// of unused tokens are discarded by the epilogue), so no MMA is predicated.
+// One 64-wide K unit for one warp's slab and NT token tiles.  Per 32-wide
+// group: the MMA chain starts from -136 * sum(x) (two MMAs of a constant
+// -136 fragment with the group's activations) and adds (q+136)*x over the
+// group's two k16 steps, giving sum(q*x) from exact products; then
+// acc += scale * chain in FP32.  Every token tile is computed (columns of
+// unused tokens are discarded by the epilogue), so no MMA is predicated.
 template <int NT>
 __device__ __forceinline__ void unit_mma(uint32_t ub, uint32_t xu, uint32_t q_off, uint32_t s_off,
-                                         const uint32_t (&neg136)[4], uint32_t mask,
-                                         uint32_t magic, float (&acc)[NT][4]) {
-  const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+                                         const SmallArgs& a, float (&acc)[NT][4]) {
   const uint4 q = lds128(ub + q_off);
   const uint2 sc = lds64(ub + s_off);
 #pragma unroll
@@ -95,16 +107,18 @@ __device__ __forceinline__ void unit_mma(uint32_t ub, uint32_t xu, uint32_t q_of
 #pragma unroll
     for (int n = 0; n < NT; ++n) ldmatrix_x4(bf[n], xu + n * 8 * kXPitch + half * 64);
     uint32_t a0[4], a1[4];
-    decode_word_offset136(half ? q.z : q.x, mask, magic, a0);
-    decode_word_offset136(half ? q.w : q.y, mask, magic, a1);
+    decode_word_offset136(half ? q.z : q.x, a.nib_mask, a.nib_magic, a0);
+    decode_word_offset136(half ? q.w : q.y, a.nib_mask, a.nib_magic, a1);
     const uint32_t sw = half ? sc.y : sc.x;
     const float s_lo = bf16lo_to_f32(sw), s_hi = bf16hi_to_f32(sw);
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
+      const uint32_t neg136[4] = {a.neg136, a.neg136, a.neg136, a.neg136};
+      const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
       float c[4];
       mma_bf16_16816(c, neg136, bf[n][0], bf[n][1], zero4);  // -136 * sum x, k 0..15
       mma_bf16_16816(c, neg136, bf[n][2], bf[n][3], c);      //            k 16..31
-      mma_bf16_16816(c, a0, bf[n][0], bf[n][1], c);          // + (q+136) x
+      mma_bf16_16816(c, a0, bf[n][0], bf[n][1], c);
       mma_bf16_16816(c, a1, bf[n][2], bf[n][3], c);
       acc[n][0] = fmaf(s_lo, c[0], acc[n][0]);
       acc[n][1] = fmaf(s_lo, c[1], acc[n][1]);
@@ -120,19 +134,22 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t item_full[kItemSlots];
+  __shared__ __align__(8) uint64_t item_empty[kItemSlots];
+  __shared__ int4 item_q[kItemSlots];   // {tile, expert, first sorted row, rows} or rows = -1: end
   __shared__ int hdr_ok;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nt = blockIdx.x, e = blockIdx.y;
-  const int cnt = __ldg(a.counts + e);
-  if (cnt == 0) return;
-  const int off = __ldg(a.offsets + e);
   if (tid == 0) {
     hdr_ok = header_ok(a);
     if (!hdr_ok) set_status(a.status, CHORD_ERR_PREPACK_MISMATCH);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    for (int q = 0; q < kItemSlots; ++q) {
+      mbar_init(&item_full[q], 1);
+      mbar_init(&item_empty[q], kConsumerWarps);
     }
     fence_mbar_init();
   }
@@ -141,43 +158,77 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
 
   const int n_units = a.K / kUnitK;
   const int k_stages = (n_units + kUnitsPerStage - 1) / kUnitsPerStage;
-  const int passes = (cnt + Cfg::kRowsPerPass - 1) / Cfg::kRowsPerPass;
-  const int iters = passes * k_stages;
-  const uint8_t* wtile = a.packed + kPackHeaderBytes +
-                         (static_cast<size_t>(e) * a.n_tiles + nt) * static_cast<size_t>(a.tile_bytes);
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    int issued = 0;
+    // Items (tile, row block), block index fastest, are taken from a global
+    // counter; each is pushed to the consumers through a small ring and its
+    // stages are streamed into the shared ring.  The last CTA to run out of
+    // items zeroes the counters for the next launch.
+    const int nblocks = __ldg(a.ntpp) / a.block_m;
+    const long long total = static_cast<long long>(a.n_tiles) * nblocks;
+    int it = 0, q = 0;
     bool ok = true;
-    for (int it = 0; it < iters && ok; ++it) {
-      const int s = it % STAGES;
-      if (it >= STAGES) ok = mbar_wait_backoff(&empty_bar[s], ((it / STAGES) - 1) & 1, a.status);
+    while (ok) {
+      int i = 0;
+      if (lane == 0) i = atomicAdd(a.work, 1);
+      i = __shfl_sync(0xffffffffu, i, 0);
+      int4 item = make_int4(0, 0, 0, -1);
+      if (i < total) {
+        const int nt = i / nblocks, b = i - nt * nblocks;
+        const int e = __ldg(a.expert_ids + b);
+        const int row0 = b * a.block_m;
+        const int rows = min(a.block_m, __ldg(a.offsets + e) + __ldg(a.counts + e) - row0);
+        item = make_int4(nt, e, row0, rows);
+      }
+      const int slot = q % kItemSlots;
+      if (q >= kItemSlots)
+        ok = mbar_wait_backoff(&item_empty[slot], ((q / kItemSlots) - 1) & 1, a.status);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
-      const int pass = it / k_stages, ks = it - pass * k_stages;
-      const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
-      const int rows = min(Cfg::kRowsPerPass, cnt - pass * Cfg::kRowsPerPass);
-      const uint32_t xbytes = units * kUnitK * 2;
-      uint8_t* st = smem + s * Cfg::kStageBytes;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&full_bar[s], units * kUnitBytes + rows * xbytes);
-        bulk_g2s(st, wtile + static_cast<size_t>(ks) * kUnitsPerStage * kUnitBytes,
-                 units * kUnitBytes, &full_bar[s]);
+        item_q[slot] = item;
+        mbar_arrive(&item_full[slot]);
       }
-      __syncwarp();
-      for (int j = lane; j < rows; j += 32) {
-        const int r = off + pass * Cfg::kRowsPerPass + j;
-        const int row = GATHER ? __ldg(a.sorted + r) / a.topk : r;
-        const uint16_t* src = a.A + static_cast<size_t>(row) * a.K + ks * kUnitsPerStage * kUnitK;
-        bulk_g2s(st + Cfg::kWBytes + j * kXPitch, src, xbytes, &full_bar[s]);
+      ++q;
+      if (item.w < 0) break;
+      const uint8_t* wtile = a.packed + kPackHeaderBytes +
+                             (static_cast<size_t>(item.y) * a.n_tiles + item.x) *
+                                 static_cast<size_t>(a.tile_bytes);
+      const int passes = (item.w + Cfg::kRowsPerPass - 1) / Cfg::kRowsPerPass;
+      for (int pass = 0; pass < passes && ok; ++pass) {
+        const int rows = min(Cfg::kRowsPerPass, item.w - pass * Cfg::kRowsPerPass);
+        for (int ks = 0; ks < k_stages; ++ks, ++it) {
+          const int s = it % STAGES;
+          if (it >= STAGES) ok = mbar_wait_backoff(&empty_bar[s], ((it / STAGES) - 1) & 1, a.status);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
+          const uint32_t xbytes = units * kUnitK * 2;
+          uint8_t* st = smem + s * Cfg::kStageBytes;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full_bar[s], units * kUnitBytes + rows * xbytes);
+            bulk_g2s(st, wtile + static_cast<size_t>(ks) * kUnitsPerStage * kUnitBytes,
+                     units * kUnitBytes, &full_bar[s]);
+          }
+          __syncwarp();
+          for (int j = lane; j < rows; j += 32) {
+            const int r = item.z + pass * Cfg::kRowsPerPass + j;
+            const int row = GATHER ? __ldg(a.sorted + r) / a.topk : r;
+            const uint16_t* src = a.A + static_cast<size_t>(row) * a.K + ks * kUnitsPerStage * kUnitK;
+            bulk_g2s(st + Cfg::kWBytes + j * kXPitch, src, xbytes, &full_bar[s]);
+          }
+        }
       }
-      issued = it + 1;
     }
-    // Before leaving, make sure no copy into this CTA's smem is in flight.
     if (lane == 0) {
-      for (int it = max(0, issued - STAGES); it < issued; ++it)
-        mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1, a.status);
+      if (ok && atomicAdd(a.work + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        atomicExch(a.work, 0);
+        atomicExch(a.work + 1, 0);
+      }
+      // Before leaving, make sure no copy into this CTA's smem is in flight.
+      for (int j = max(0, it - STAGES); j < it; ++j)
+        mbar_wait(&full_bar[j % STAGES], (j / STAGES) & 1, a.status);
     }
     return;
   }
@@ -188,54 +239,59 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
   const uint32_t q_off = warp * 512 + lane * 16;             // this warp's slab, this lane
   const uint32_t s_off = kUnitQBytes + warp * 64 + g * 8;
   const uint32_t x_off = Cfg::kWBytes + (lane & 7) * kXPitch + (lane >> 3) * 16;
-  const uint32_t neg136[4] = {a.neg136, a.neg136, a.neg136, a.neg136};
-  const uint32_t mask = a.nib_mask, magic = a.nib_magic;
-  for (int pass = 0; pass < passes; ++pass) {
-    const int rows = min(Cfg::kRowsPerPass, cnt - pass * Cfg::kRowsPerPass);
-    float acc[NT][4];
+  int it = 0;
+  for (int q = 0;; ++q) {
+    const int slot = q % kItemSlots;
+    if (!mbar_wait(&item_full[slot], (q / kItemSlots) & 1, a.status)) return;
+    const int4 item = item_q[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&item_empty[slot]);
+    if (item.w < 0) return;
+    const int passes = (item.w + Cfg::kRowsPerPass - 1) / Cfg::kRowsPerPass;
+    for (int pass = 0; pass < passes; ++pass) {
+      const int rows = min(Cfg::kRowsPerPass, item.w - pass * Cfg::kRowsPerPass);
+      float acc[NT][4];
 #pragma unroll
-    for (int n = 0; n < NT; ++n)
+      for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
+        for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
 
-    for (int ks = 0; ks < k_stages; ++ks) {
-      const int it = pass * k_stages + ks;
-      const int s = it % STAGES;
-      if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status)) return;
-      const uint32_t st = smem_base + s * Cfg::kStageBytes;
-      const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
-      if (units == kUnitsPerStage) {
+      for (int ks = 0; ks < k_stages; ++ks, ++it) {
+        const int s = it % STAGES;
+        if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status)) return;
+        const uint32_t st = smem_base + s * Cfg::kStageBytes;
+        const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
+        if (units == kUnitsPerStage) {
 #pragma unroll
-        for (int u = 0; u < kUnitsPerStage; ++u)
-          unit_mma<NT>(st + u * kUnitBytes, st + x_off + u * kUnitK * 2, q_off, s_off, neg136, mask,
-                       magic, acc);
-      } else {
-#pragma unroll 1
-        for (int u = 0; u < units; ++u)
-          unit_mma<NT>(st + u * kUnitBytes, st + x_off + u * kUnitK * 2, q_off, s_off, neg136, mask,
-                       magic, acc);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);
-    }
-
-    // ------------------------------------------------------------ epilogue
-    const size_t r0 = static_cast<size_t>(off) + pass * Cfg::kRowsPerPass;
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int tok = n * 8 + 2 * t + i;
-        if (tok >= rows) continue;
-        uint16_t* crow = a.C + (r0 + tok) * a.ldc;
-        if (EPI == CHORD_EPI_SILU_MUL) {
-          // acc[n][i]: gate of index i0 + g; acc[n][2 + i]: up of the same index
-          const int col = 32 * nt + 8 * warp + g;
-          crow[col] = f32_to_bf16_rn(silu_f32(acc[n][i]) * acc[n][2 + i]);
+          for (int u = 0; u < kUnitsPerStage; ++u)
+            unit_mma<NT>(st + u * kUnitBytes, st + x_off + u * kUnitK * 2, q_off, s_off, a, acc);
         } else {
-          const int col = kTileRows * nt + 16 * warp + g;
-          if (col < a.N) crow[col] = f32_to_bf16_rn(acc[n][i]);
-          if (col + 8 < a.N) crow[col + 8] = f32_to_bf16_rn(acc[n][2 + i]);
+#pragma unroll 1
+          for (int u = 0; u < units; ++u)
+            unit_mma<NT>(st + u * kUnitBytes, st + x_off + u * kUnitK * 2, q_off, s_off, a, acc);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
+
+      // ---------------------------------------------------------- epilogue
+      const size_t r0 = static_cast<size_t>(item.z) + pass * Cfg::kRowsPerPass;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int tok = n * 8 + 2 * t + i;
+          if (tok >= rows) continue;
+          uint16_t* crow = a.C + (r0 + tok) * a.ldc;
+          if (EPI == CHORD_EPI_SILU_MUL) {
+            // acc[n][i]: gate of index i0 + g; acc[n][2 + i]: up of the same index
+            const int col = 32 * item.x + 8 * warp + g;
+            crow[col] = f32_to_bf16_rn(silu_f32(acc[n][i]) * acc[n][2 + i]);
+          } else {
+            const int col = kTileRows * item.x + 16 * warp + g;
+            if (col < a.N) crow[col] = f32_to_bf16_rn(acc[n][i]);
+            if (col + 8 < a.N) crow[col + 8] = f32_to_bf16_rn(acc[n][2 + i]);
+          }
         }
       }
     }
@@ -245,10 +301,24 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
 template <int NT, int STAGES, bool GATHER, int EPI>
 cudaError_t launch_small(const SmallArgs& a, cudaStream_t st) {
   const int smem = STAGES * SmallCfg<NT>::kStageBytes;
+  auto kern = gemm_small_kernel<NT, STAGES, GATHER, EPI>;
   cudaError_t err = ensure_smem_limit<gemm_small_kernel<NT, STAGES, GATHER, EPI>>(smem);
   if (err != cudaSuccess) return err;
-  dim3 grid(a.n_tiles, a.E_local);
-  gemm_small_kernel<NT, STAGES, GATHER, EPI><<<grid, kThreads, smem, st>>>(a);
+  static int per_sm[64] = {0}, sms[64] = {0};
+  int dev = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!per_sm[dev]) {
+    int n = 0, m = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&m, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    sms[dev] = m;
+    per_sm[dev] = n > 0 ? n : 1;
+  }
+  gemm_small_kernel<NT, STAGES, GATHER, EPI><<<per_sm[dev] * sms[dev], kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -269,8 +339,12 @@ cudaError_t gemm_small_launch(const GemmLaunch& g, int rows_per_pass, cudaStream
   a.A = g.A;
   a.packed = static_cast<const uint8_t*>(g.packed);
   a.sorted = g.sorted;
+  a.expert_ids = g.expert_ids;
+  a.ntpp = g.ntpp;
   a.counts = g.counts;
   a.offsets = g.offsets;
+  a.work = g.work;
+  a.block_m = g.block_m;
   a.C = g.C;
   a.status = g.status;
   a.N = g.N;

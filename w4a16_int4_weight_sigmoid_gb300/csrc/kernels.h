@@ -32,13 +32,21 @@ struct GemmLaunch {
   const void* packed;
   int E_local, N, K, M, topk;
   const int32_t* sorted;
+  const int32_t* expert_ids;
+  const int32_t* ntpp;
   const int32_t* counts;
   const int32_t* offsets;
+  int block_m;
+  int* work;        // small-M path: 2 ints, zero before the first launch (kept zero)
   int epilogue;
   uint16_t* C;
   int* status;
 };
 cudaError_t gemm_small_launch(const GemmLaunch& g, int rows_per_pass, cudaStream_t st);
+size_t gemm_large_smem_bytes();
+cudaError_t gemm_large_launch(const GemmLaunch& g, const uint16_t* B, size_t b_rows, cudaStream_t st);
+cudaError_t gather_rows_launch(const uint16_t* x, const int32_t* sorted, const int32_t* ntpp, int topk,
+                               int sentinel, int K, size_t capacity, uint16_t* out, cudaStream_t st);
 
 cudaError_t moe_sum_launch(const uint16_t* y, const float* w, const int32_t* pos, int M, int topk,
                            int H, uint16_t* out, cudaStream_t st);
