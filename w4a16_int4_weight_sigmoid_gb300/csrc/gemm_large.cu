@@ -4,23 +4,35 @@
 // pipeline gives the better throughput; [Chord] "그룹 SM90 커널 기법": a
 // persistent warp-specialised main loop pipelining TMA loads, dequantisation
 // and the MMA.  Design on sm_103a (one CTA per SM, persistent):
-//   * work item = (local expert, 128 weight rows, pass of up to 256 of the
-//     expert's rows); items are dealt round-robin to the CTAs;
+//   * work item = (local expert, 128 weight rows, pass of up to 192 of the
+//     expert's rows); items are dealt round-robin to the CTAs, so the CTAs
+//     running at one time cover a few experts and their activation rows
+//     stay in L2;
 //   * the MMA is "swap AB": the 128 weight rows are M, the expert's rows
-//     (tokens) are N (a multiple of 16 up to 256), so an expert's rows are
+//     (tokens) are N (a multiple of 16 up to 192), so an expert's rows are
 //     padded to 16, not to 128;
-//   * warp 0 (producer): 1-D bulk copies of the two packed 64-row units of
-//     each 64-wide K step, and 2-D TMA loads (128-byte swizzle) of the
-//     expert's activation rows, into a 4-stage ring;
-//   * warps 2-5 (dequant): INT4 -> BF16 q*s (rounded once) written into the
-//     K-major 128-byte-swizzled A tile, then a proxy fence;
-//   * warp 1 (MMA): TMEM allocation, one thread issues tcgen05.mma
-//     (M=128, K=16 x4 per stage) into one of two TMEM accumulators and
-//     commits stage and item completion to mbarriers;
-//   * warps 6-9 (epilogue): tcgen05.ld of the accumulator, SiLU(gate) * up
+//   * the dequantised weights (A) never touch shared memory: the dequant
+//     warps write them into tensor memory with tcgen05.st (the packed
+//     fragment order is the 16x128b store order) and tcgen05.mma reads A
+//     from TMEM; only the activations (B) are read from shared memory, which
+//     halves the shared-memory traffic per MMA;
+//   * one pipeline stage is 128 of K (eight K=16 MMAs), so every mbarrier
+//     handshake covers twice the tensor work of a 64-wide stage;
+//   * three rings, each with its own full/empty mbarriers: packed weights
+//     (shared memory, 6 deep, from HBM, 1-D bulk copies by warp 0),
+//     activation tiles (shared memory, 3 deep, from L2, one 2-D TMA box of
+//     up to 192 rows per 64 of K, 128-byte swizzle, by warp 2) and
+//     dequantised A tiles (TMEM, 2 deep);
+//   * warps 4-11 (dequant, one 32-row TMEM lane quarter and one 64-wide half
+//     of the stage each): INT4 -> BF16 q*s (rounded once), tcgen05.st;
+//   * warp 1 (MMA): TMEM allocation; one thread issues the MMAs (M=128) into
+//     one of two accumulators and commits slot release and item completion
+//     to mbarriers;
+//   * warps 12-15 (epilogue): tcgen05.ld of the accumulator, SiLU(gate) * up
 //     (gate and up rows of one index sit 8 TMEM lanes apart) or a plain
 //     store, BF16, rows in sorted order; the second accumulator lets the next
 //     item's MMAs run meanwhile.
+// TMEM: accumulators at columns 0 and 192, A slots at 384 and 448.
 // Every mbarrier wait is bounded; on a timeout the CTA records
 // CHORD_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include "common.cuh"
@@ -30,19 +42,27 @@
 namespace chord {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kMRows = 128;                      // weight rows per item (2 packed tiles)
-constexpr int kMaxTok = 256;                     // tokens per pass (MMA N)
-constexpr int kBoxRows = 32;                     // activation rows per TMA box
-constexpr int kABytes = kMRows * kUnitK * 2;     // 16 KB
-constexpr int kBBytes = kMaxTok * kUnitK * 2;    // 32 KB
-constexpr int kPBytes = 2 * kUnitBytes;          // 4608
-constexpr int kStageBytes = kABytes + kBBytes + 5120;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
-constexpr int kThreads = 320;
+constexpr int kMaxTok = 192;                     // tokens per pass (MMA N)
+constexpr int kStageUnits = 2;                   // 64-wide K units per stage
+constexpr int kSP = 6, kSB = 3, kSA = 2;         // ring depths: packed, activations, A in TMEM
+constexpr int kBHalfBytes = kMaxTok * kUnitK * 2;            // 24 KB: 192 rows x 128 B
+constexpr int kBStageBytes = kStageUnits * kBHalfBytes;      // 48 KB
+constexpr int kPStageBytes = 2 * kStageUnits * kUnitBytes;   // 9216: [tile][unit]
+constexpr int kBOff = 0, kPOff = kSB * kBStageBytes;
+constexpr int kSmemBytes = kPOff + kSP * kPStageBytes + 1024;   // + alignment slack
+constexpr int kAccCols = kMaxTok;                // accumulator j at column j * 192
+constexpr int kACol0 = 2 * kAccCols;             // A slot s at column 384 + 64 s
+constexpr int kASlotCols = kStageUnits * kUnitK / 2;         // 64
 constexpr int kTmemCols = 512;
+static_assert(kACol0 + kSA * kASlotCols <= kTmemCols, "TMEM budget");
+constexpr int kDequantWarp0 = 4, kDequantWarps = 8;
+constexpr int kEpiWarp0 = kDequantWarp0 + kDequantWarps;   // 12: warp index % 4 = lane quarter
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kMaxExperts = 1024;
-static_assert(kSmemBytes + (kMaxExperts + 1) * 4 + 256 <= 232448, "shared memory budget");
+static_assert(kSmemBytes + (kMaxExperts + 1) * 4 + 512 <= 232448, "shared memory budget");
+static_assert((kBHalfBytes % 1024) == 0 && (kPOff % 1024) == 0, "SW128 tiles");
+static_assert((kDequantWarp0 % 4) == 0 && (kEpiWarp0 % 4) == 0, "warp index selects the TMEM lane quarter");
 
 struct LargeArgs {
   const uint8_t* packed;
@@ -54,6 +74,8 @@ struct LargeArgs {
   int64_t tile_bytes;
   uint32_t need_flags;
   int gate_up;
+  int box_s, box_b;               // activation box heights (rows): small items / the rest
+  uint32_t nib_mask, nib_magic;   // decode constants, passed at run time so they stay in registers
 };
 
 struct Item {
@@ -89,10 +111,19 @@ __device__ __forceinline__ Item item_of(int i, const int* prefix, const int32_t*
   return it;
 }
 
+// 64-wide K units in stage ks (the last stage of a K that is an odd number
+// of units holds one).
+__device__ __forceinline__ int stage_units(int ks, int n_units) {
+  return min(kStageUnits, n_units - ks * kStageUnits);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_large_kernel(const __grid_constant__ CUtensorMap tmap_b, LargeArgs a) {
+    gemm_large_kernel(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_b,
+                      LargeArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kStages], afull_bar[kStages], empty_bar[kStages];
+  __shared__ __align__(8) uint64_t p_full[kSP], p_empty[kSP];
+  __shared__ __align__(8) uint64_t b_full[kSB], b_empty[kSB];
+  __shared__ __align__(8) uint64_t a_full[kSA], a_empty[kSA];
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], done_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int prefix[kMaxExperts + 1];
@@ -102,18 +133,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t smem0 = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (smem0 - smem_u32(smem_raw));
-  const int E = a.E_local, K = a.K;
+  const int E = a.E_local;
   const int n_wt = a.N / kMRows;
-  const int k_steps = K / kUnitK;
+  const int n_units = a.K / kUnitK;
+  const int n_stages = (n_units + kStageUnits - 1) / kStageUnits;
 
   if (tid == 0) {
     hdr_ok = header_ok(a);
     if (!hdr_ok) set_status(a.status, CHORD_ERR_PREPACK_MISMATCH);
     abort_flag = 0;
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&afull_bar[s], 4);
-      mbar_init(&empty_bar[s], 1);
+    for (int s = 0; s < kSP; ++s) {
+      mbar_init(&p_full[s], 1);
+      mbar_init(&p_empty[s], kDequantWarps);
+    }
+    for (int s = 0; s < kSB; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < kSA; ++s) {
+      mbar_init(&a_full[s], kDequantWarps);
+      mbar_init(&a_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -149,35 +188,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_items = hdr_ok ? prefix[E] : 0;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------ packed-weight producer
     if (lane == 0) {
       int it = 0;
       for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x) {
         const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
-        const int nbox = (item.rows + kBoxRows - 1) / kBoxRows;
         const uint8_t* t0 = a.packed + kPackHeaderBytes +
                             (static_cast<size_t>(item.e) * a.n_blob_tiles + 2 * item.wt) *
                                 static_cast<size_t>(a.tile_bytes);
-        for (int ks = 0; ks < k_steps; ++ks, ++it) {
-          const int s = it % kStages;
-          if (it >= kStages && !mbar_wait(&empty_bar[s], ((it / kStages) - 1) & 1, a.status)) {
+        for (int ks = 0; ks < n_stages; ++ks, ++it) {
+          const int s = it % kSP;
+          if (it >= kSP && !mbar_wait_backoff(&p_empty[s], ((it / kSP) - 1) & 1, a.status)) {
             abort_flag = 1;
             break;
           }
-          uint8_t* st = smem + s * kStageBytes;
-          mbar_arrive_expect_tx(&full_bar[s], kPBytes + nbox * kBoxRows * kUnitK * 2);
-          bulk_g2s(st + kABytes + kBBytes, t0 + static_cast<size_t>(ks) * kUnitBytes, kUnitBytes,
-                   &full_bar[s]);
-          bulk_g2s(st + kABytes + kBBytes + kUnitBytes,
-                   t0 + a.tile_bytes + static_cast<size_t>(ks) * kUnitBytes, kUnitBytes, &full_bar[s]);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(st + kABytes + b * kBoxRows * kUnitK * 2, &tmap_b, ks * kUnitK,
-                        item.row0 + b * kBoxRows, &full_bar[s]);
+          const uint32_t bytes = stage_units(ks, n_units) * kUnitBytes;
+          const size_t src = static_cast<size_t>(ks) * kStageUnits * kUnitBytes;
+          uint8_t* dst = smem + kPOff + s * kPStageBytes;
+          mbar_arrive_expect_tx(&p_full[s], 2 * bytes);
+          bulk_g2s(dst, t0 + src, bytes, &p_full[s]);
+          bulk_g2s(dst + kStageUnits * kUnitBytes, t0 + a.tile_bytes + src, bytes, &p_full[s]);
         }
       }
       // drain: every issued copy must land before the CTA can exit
-      for (int j = max(0, it - kStages); j < it; ++j)
-        mbar_wait(&full_bar[j % kStages], (j / kStages) & 1, a.status);
+      for (int j = max(0, it - kSP); j < it; ++j)
+        mbar_wait(&p_full[j % kSP], (j / kSP) & 1, a.status);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------- activation producer
+    if (lane == 0) {
+      int it = 0;
+      for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x) {
+        const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
+        const int n_mma = (item.rows + 15) & ~15;
+        const bool small = n_mma <= a.box_s;
+        const CUtensorMap* map = small ? &map_s : &map_b;
+        const int box = small ? a.box_s : a.box_b;
+        const int nbox = (n_mma + box - 1) / box;   // box divides 192: nbox * box <= 192
+        for (int ks = 0; ks < n_stages; ++ks, ++it) {
+          const int s = it % kSB;
+          if (it >= kSB && !mbar_wait_backoff(&b_empty[s], ((it / kSB) - 1) & 1, a.status)) {
+            abort_flag = 1;
+            break;
+          }
+          const int nu = stage_units(ks, n_units);
+          uint8_t* dst = smem + kBOff + s * kBStageBytes;
+          mbar_arrive_expect_tx(&b_full[s], nu * nbox * box * kUnitK * 2);
+          for (int h = 0; h < nu; ++h)
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(dst + h * kBHalfBytes + b * box * kUnitK * 2, map,
+                          (ks * kStageUnits + h) * kUnitK, item.row0 + b * box, &b_full[s]);
+        }
+      }
+      for (int j = max(0, it - kSB); j < it; ++j)
+        mbar_wait(&b_full[j % kSB], (j / kSB) & 1, a.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -194,22 +258,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int n_mma = (item.rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(kMRows, n_mma);
-        const uint32_t d_tmem = tmem_base + acc * kMaxTok;
-        for (int ks = 0; ks < k_steps; ++ks, ++it) {
-          const int s = it % kStages;
-          if (!mbar_wait(&afull_bar[s], (it / kStages) & 1, a.status) ||
-              !mbar_wait(&full_bar[s], (it / kStages) & 1, a.status)) {
+        const uint32_t d_tmem = tmem_base + acc * kAccCols;
+        for (int ks = 0; ks < n_stages; ++ks, ++it) {
+          const int sa = it % kSA, sb = it % kSB;
+          if (!mbar_wait(&a_full[sa], (it / kSA) & 1, a.status) ||
+              !mbar_wait(&b_full[sb], (it / kSB) & 1, a.status)) {
             abort_flag = 1;
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem0 + s * kStageBytes;
-          const uint64_t a_desc = sw128_kmajor_desc(st);
-          const uint64_t b_desc = sw128_kmajor_desc(st + kABytes);
-#pragma unroll
-          for (int kk = 0; kk < kUnitK / 16; ++kk)
-            tc_mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, (ks | kk) != 0);
-          tc_commit(&empty_bar[s]);
+          const uint32_t a_tmem = tmem_base + kACol0 + sa * kASlotCols;
+          const uint32_t b_base = smem0 + kBOff + sb * kBStageBytes;
+          const int nk = 4 * stage_units(ks, n_units);
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint64_t b_desc = sw128_kmajor_desc(b_base + (kk >> 2) * kBHalfBytes) + 2 * (kk & 3);
+            tc_mma_bf16_ts(d_tmem, a_tmem + 8 * kk, b_desc, idesc, (ks | kk) != 0);
+          }
+          tc_commit(&a_empty[sa]);
+          tc_commit(&b_empty[sb]);
           issued_any = true;
         }
         if (abort_flag) break;
@@ -221,73 +287,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&done_bar, 0, a.status);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp >= kDequantWarp0 && warp < kEpiWarp0) {
     // ------------------------------------------------------------ dequant
-    const int d = warp - 2;
-    const int g = lane >> 2, t = lane & 3;
-    const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;
+    // This warp: TMEM lane quarter q (rows 32q..32q+31 = slabs 2q, 2q+1 of
+    // the 128-row item) and unit hu (K 64*hu .. 64*hu+63) of each stage.
+    const int dq = warp - kDequantWarp0;
+    const int q = warp & 3, hu = dq >> 2;
+    const int g = lane >> 2;
+    const uint32_t mask = a.nib_mask, magic = a.nib_magic;   // run-time: kept in registers
     const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.f, 136.f);
+    // packed offsets of slab sl (0, 1) within a stage: tile, unit, slab-in-tile
+    uint32_t q_off[2], s_off[2];
+#pragma unroll
+    for (int sl = 0; sl < 2; ++sl) {
+      const int s = 2 * q + sl;   // slab of the 128-row item
+      const uint32_t unit = ((s >> 2) * kStageUnits + hu) * kUnitBytes;
+      q_off[sl] = kPOff + unit + (s & 3) * 512 + lane * 16;
+      s_off[sl] = kPOff + unit + kUnitQBytes + (s & 3) * 64 + g * 8;
+    }
+    const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
     int it = 0;
     for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x) {
-      for (int ks = 0; ks < k_steps; ++ks, ++it) {
-        const int s = it % kStages;
-        if (!mbar_wait(&full_bar[s], (it / kStages) & 1, a.status)) {
+      for (int ks = 0; ks < n_stages; ++ks, ++it) {
+        const int sp = it % kSP, sa = it % kSA;
+        if (!mbar_wait(&p_full[sp], (it / kSP) & 1, a.status) ||
+            (it >= kSA && !mbar_wait(&a_empty[sa], ((it / kSA) - 1) & 1, a.status))) {
           abort_flag = 1;
           break;
         }
-        uint8_t* st = smem + s * kStageBytes;
-        const uint8_t* pk = st + kABytes + kBBytes;
+        tc_fence_after();
+        const bool active = hu < stage_units(ks, n_units);
+        uint32_t v[2][16];
+        if (active) {
+          const uint8_t* pst = smem + sp * kPStageBytes;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int S = 2 * d + h;                      // 16-row slab of the 128-row tile
-          const uint8_t* unit = pk + (S >> 2) * kUnitBytes;
-          const uint4 q = *reinterpret_cast<const uint4*>(unit + (S & 3) * 512 + lane * 16);
-          const uint2 sc = *reinterpret_cast<const uint2*>(unit + kUnitQBytes + (S & 3) * 64 + g * 8);
-          const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-          const int r_lo = 16 * S + g;                  // rows r_lo and r_lo + 8; (row & 7) == g
+          for (int sl = 0; sl < 2; ++sl) {
+            const uint4 qw = *reinterpret_cast<const uint4*>(pst + q_off[sl]);
+            const uint2 sc = *reinterpret_cast<const uint2*>(pst + s_off[sl]);
+            const uint32_t w4[4] = {qw.x, qw.y, qw.z, qw.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t sw = (j >> 1) ? sc.y : sc.x;
-            const uint32_t s_lo = __byte_perm(sw, sw, 0x1010);   // {s[g], s[g]}
-            const uint32_t s_hi = __byte_perm(sw, sw, 0x3232);   // {s[g+8], s[g+8]}
-            uint32_t v[4];
-            decode_word_offset136(w4[j], mask, magic, v);
+            for (int j = 0; j < 4; ++j) {   // K=16 step j; scale group j / 2
+              const uint32_t sw = (j >> 1) ? sc.y : sc.x;
+              const uint32_t s_lo = __byte_perm(sw, sw, 0x1010);   // {s[g], s[g]}
+              const uint32_t s_hi = __byte_perm(sw, sw, 0x3232);   // {s[g+8], s[g+8]}
+              uint32_t d[4];
+              decode_word_offset136(w4[j], mask, magic, d);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&v[r]);
-              x = __hsub2(x, k136);
-              const uint32_t sr = (r & 1) ? s_hi : s_lo;
-              x = __hmul2(x, *reinterpret_cast<const __nv_bfloat162*>(&sr));
-              v[r] = *reinterpret_cast<uint32_t*>(&x);
-            }
-            // v[0]: row r_lo, k 16j+2t; v[1]: row r_lo+8; v[2]: row r_lo, k +8; v[3]: row r_lo+8, k +8
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const int row = r_lo + 8 * (r & 1);
-              const int chunk = 2 * j + (r >> 1);
-              const uint32_t off = row * 128 + ((chunk ^ g) << 4) + 4 * t;
-              *reinterpret_cast<uint32_t*>(st + off) = v[r];
+              for (int r = 0; r < 4; ++r) {   // d[r]: fragment register a_r (rows g, g+8, g, g+8)
+                __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&d[r]);
+                x = __hsub2(x, k136);
+                const uint32_t sr = (r & 1) ? s_hi : s_lo;
+                x = __hmul2(x, *reinterpret_cast<const __nv_bfloat162*>(&sr));
+                v[sl][4 * j + r] = *reinterpret_cast<uint32_t*>(&x);
+              }
             }
           }
         }
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull_bar[s]);
+        if (lane == 0) mbar_arrive(&p_empty[sp]);     // packed data consumed into registers
+        if (active) {
+          const uint32_t col = tmem_base + kACol0 + sa * kASlotCols + hu * (kUnitK / 2);
+          tmem_st_16x128b_x8(col + t_lane, v[0]);
+          tmem_st_16x128b_x8(col + t_lane + (16u << 16), v[1]);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[sa]);
       }
     }
-  } else {
+  } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
     const int qw = warp & 3;                 // TMEM lane quarter of this warp
     int j = 0;
     for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x, ++j) {
       const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
       const int acc = j & 1, use = j >> 1;
-      if (!mbar_wait(&tfull_bar[acc], use & 1, a.status)) {
+      if (!mbar_wait_backoff(&tfull_bar[acc], use & 1, a.status)) {
         abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + acc * kMaxTok + (static_cast<uint32_t>(32 * qw) << 16);
+      const uint32_t taddr = tmem_base + acc * kAccCols + (static_cast<uint32_t>(32 * qw) << 16);
       const int row_in = 32 * qw + lane;     // A row = TMEM lane
       for (int c0 = 0; c0 < item.rows; c0 += 32) {
         uint32_t v[32];
@@ -351,24 +432,39 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// Activation tensor map: rows of K BF16 (row stride 2K bytes), boxes of 64
+// along K by `box_rows` rows, 128-byte swizzle.
+bool encode_b_map(EncodeTiledFn encode, CUtensorMap* map, const uint16_t* B, int K, size_t rows,
+                  int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kUnitK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(B), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 size_t gemm_large_smem_bytes() { return kSmemBytes; }
 
 cudaError_t gemm_large_launch(const GemmLaunch& g, const uint16_t* B, size_t b_rows,
                               cudaStream_t st) {
-  if (g.N % kMRows != 0 || g.K % kUnitK != 0 || g.E_local > kMaxExperts) return cudaErrorInvalidValue;
+  if (g.N % kMRows != 0 || g.K % kUnitK != 0 || g.E_local > kMaxExperts || b_rows < 8)
+    return cudaErrorInvalidValue;
   EncodeTiledFn encode = get_encode_fn();
   if (!encode) return cudaErrorNotSupported;
-  CUtensorMap map;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.K), static_cast<cuuint64_t>(b_rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.K) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kUnitK), static_cast<cuuint32_t>(kBoxRows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(B), dims,
-                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // Box heights divide 192 (the activation slot), so whole boxes never
+  // overrun a slot; rows past the tensor's end read as zeros.
+  int box_s = 8;
+  for (int r : {64, 32, 16})
+    if (b_rows >= static_cast<size_t>(r)) { box_s = r; break; }
+  const int box_b = b_rows >= static_cast<size_t>(kMaxTok) ? kMaxTok : box_s;
+  CUtensorMap map_s, map_b;
+  if (!encode_b_map(encode, &map_s, B, g.K, b_rows, box_s) ||
+      !encode_b_map(encode, &map_b, B, g.K, b_rows, box_b))
+    return cudaErrorInvalidValue;
   LargeArgs a;
   a.packed = static_cast<const uint8_t*>(g.packed);
   a.counts = g.counts;
@@ -385,12 +481,16 @@ cudaError_t gemm_large_launch(const GemmLaunch& g, const uint16_t* B, size_t b_r
   a.need_flags = gate_up ? kPackFlagGateUp : 0u;
   a.gate_up = gate_up ? 1 : 0;
   a.ldc = gate_up ? g.N / 2 : g.N;
+  a.box_s = box_s;
+  a.box_b = box_b;
+  a.nib_mask = 0x000F000Fu;
+  a.nib_magic = 0x43004300u;
   cudaError_t err = ensure_smem_limit<gemm_large_kernel>(kSmemBytes);
   if (err != cudaSuccess) return err;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  gemm_large_kernel<<<sms, kThreads, kSmemBytes, st>>>(map, a);
+  gemm_large_kernel<<<sms, kThreads, kSmemBytes, st>>>(map_s, map_b, a);
   return cudaGetLastError();
 }
 
