@@ -25,9 +25,9 @@
 //     dequantised A tiles (TMEM, 2 deep);
 //   * warps 4-11 (dequant, one 32-row TMEM lane quarter and one 64-wide half
 //     of the stage each): INT4 -> BF16 q*s (rounded once), tcgen05.st;
-//   * warp 1 (MMA): TMEM allocation; one thread issues the MMAs (M=128) into
-//     one of two accumulators and commits slot release and item completion
-//     to mbarriers;
+//   * warp 1 (MMA): TMEM allocation; the converged warp waits and one
+//     elected lane issues the MMAs (M=128) into one of two accumulators and
+//     commits slot release and item completion to mbarriers;
 //   * warps 12-15 (epilogue): tcgen05.ld of the accumulator, SiLU(gate) * up
 //     (gate and up rows of one index sit 8 TMEM lanes apart) or a plain
 //     store, BF16, rows in sorted order; the second accumulator lets the next
@@ -78,6 +78,25 @@ struct LargeArgs {
   uint32_t nib_mask, nib_magic;   // decode constants, passed at run time so they stay in registers
 };
 
+// tcgen05.mma / commit issued by one elected lane of a converged warp (the
+// operands are warp-uniform), which keeps the issue path short.
+__device__ __forceinline__ void mma_ts_elect(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred q, e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "setp.ne.b32 q, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
 struct Item {
   int e, wt, row0, rows;
 };
@@ -109,6 +128,37 @@ __device__ __forceinline__ Item item_of(int i, const int* prefix, const int32_t*
   it.row0 = __ldg(offsets + e) + p * tp;
   it.rows = min(tp, cnt - p * tp);
   return it;
+}
+
+// Dequantise this lane's part of two 16-row slabs of one 64-wide K unit
+// (packed fragment order) into BF16 q*s pairs, 16 registers per slab in the
+// tcgen05.st 16x128b order: per K=16 step j, fragment registers a0..a3.
+__device__ __forceinline__ void dequant_two_slabs(const uint8_t* pst, const uint32_t (&q_off)[2],
+                                                  const uint32_t (&s_off)[2], uint32_t mask, uint32_t magic,
+                                                  uint32_t (&v)[2][16]) {
+  const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.f, 136.f);
+#pragma unroll
+  for (int sl = 0; sl < 2; ++sl) {
+    const uint4 qw = *reinterpret_cast<const uint4*>(pst + q_off[sl]);
+    const uint2 sc = *reinterpret_cast<const uint2*>(pst + s_off[sl]);
+    const uint32_t w4[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // K=16 step j; scale group j / 2
+      const uint32_t sw = (j >> 1) ? sc.y : sc.x;
+      const uint32_t s_lo = __byte_perm(sw, sw, 0x1010);   // {s[g], s[g]}
+      const uint32_t s_hi = __byte_perm(sw, sw, 0x3232);   // {s[g+8], s[g+8]}
+      uint32_t d[4];
+      decode_word_offset136(w4[j], mask, magic, d);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {   // d[r]: fragment register a_r (rows g, g+8, g, g+8)
+        __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&d[r]);
+        x = __hsub2(x, k136);
+        const uint32_t sr = (r & 1) ? s_hi : s_lo;
+        x = __hmul2(x, *reinterpret_cast<const __nv_bfloat162*>(&sr));
+        v[sl][4 * j + r] = *reinterpret_cast<uint32_t*>(&x);
+      }
+    }
+  }
 }
 
 // 64-wide K units in stage ks (the last stage of a K that is an odd number
@@ -245,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (all lanes wait on the same barriers);
+    // one elected lane issues each MMA and commit.
+    {
       int it = 0, j = 0;
       bool issued_any = false;
       for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x, ++j) {
@@ -269,21 +321,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a_tmem = tmem_base + kACol0 + sa * kASlotCols;
           const uint32_t b_base = smem0 + kBOff + sb * kBStageBytes;
-          const int nk = 4 * stage_units(ks, n_units);
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint64_t b_desc = sw128_kmajor_desc(b_base + (kk >> 2) * kBHalfBytes) + 2 * (kk & 3);
-            tc_mma_bf16_ts(d_tmem, a_tmem + 8 * kk, b_desc, idesc, (ks | kk) != 0);
+          const uint64_t bd0 = sw128_kmajor_desc(b_base);
+          const uint32_t acc0 = ks != 0 ? 1u : 0u;
+          if (stage_units(ks, n_units) == kStageUnits) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts_elect(d_tmem, a_tmem + 8 * kk, bd0 + (kk >> 2) * (kBHalfBytes >> 4) + 2 * (kk & 3), idesc,
+                             kk ? 1u : acc0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts_elect(d_tmem, a_tmem + 8 * kk, bd0 + 2 * kk, idesc, kk ? 1u : acc0);
           }
-          tc_commit(&a_empty[sa]);
-          tc_commit(&b_empty[sb]);
+          commit_elect(&a_empty[sa]);
+          commit_elect(&b_empty[sb]);
           issued_any = true;
         }
         if (abort_flag) break;
-        tc_commit(&tfull_bar[acc]);
+        commit_elect(&tfull_bar[acc]);
       }
       // all issued MMAs complete before TMEM can be freed
       if (issued_any) {
-        tc_commit(&done_bar);
+        commit_elect(&done_bar);
         mbar_wait(&done_bar, 0, a.status);
       }
     }
@@ -295,54 +354,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, hu = dq >> 2;
     const int g = lane >> 2;
     const uint32_t mask = a.nib_mask, magic = a.nib_magic;   // run-time: kept in registers
-    const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.f, 136.f);
     // packed offsets of slab sl (0, 1) within a stage: tile, unit, slab-in-tile
     uint32_t q_off[2], s_off[2];
 #pragma unroll
     for (int sl = 0; sl < 2; ++sl) {
-      const int s = 2 * q + sl;   // slab of the 128-row item
-      const uint32_t unit = ((s >> 2) * kStageUnits + hu) * kUnitBytes;
-      q_off[sl] = kPOff + unit + (s & 3) * 512 + lane * 16;
-      s_off[sl] = kPOff + unit + kUnitQBytes + (s & 3) * 64 + g * 8;
+      const int sb = 2 * q + sl;   // slab of the 128-row item
+      const uint32_t unit = ((sb >> 2) * kStageUnits + hu) * kUnitBytes;
+      q_off[sl] = kPOff + unit + (sb & 3) * 512 + lane * 16;
+      s_off[sl] = kPOff + unit + kUnitQBytes + (sb & 3) * 64 + g * 8;
     }
     const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
     int it = 0;
     for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x) {
       for (int ks = 0; ks < n_stages; ++ks, ++it) {
         const int sp = it % kSP, sa = it % kSA;
-        if (!mbar_wait(&p_full[sp], (it / kSP) & 1, a.status) ||
-            (it >= kSA && !mbar_wait(&a_empty[sa], ((it / kSA) - 1) & 1, a.status))) {
+        bool ok = mbar_wait(&p_full[sp], (it / kSP) & 1, a.status) &&
+                  (it < kSA || mbar_wait(&a_empty[sa], ((it / kSA) - 1) & 1, a.status));
+        ok = __all_sync(0xffffffffu, ok);   // warp-uniform: the .sync.aligned work below
+        if (!ok) {
           abort_flag = 1;
           break;
         }
         tc_fence_after();
         const bool active = hu < stage_units(ks, n_units);
         uint32_t v[2][16];
-        if (active) {
-          const uint8_t* pst = smem + sp * kPStageBytes;
-#pragma unroll
-          for (int sl = 0; sl < 2; ++sl) {
-            const uint4 qw = *reinterpret_cast<const uint4*>(pst + q_off[sl]);
-            const uint2 sc = *reinterpret_cast<const uint2*>(pst + s_off[sl]);
-            const uint32_t w4[4] = {qw.x, qw.y, qw.z, qw.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {   // K=16 step j; scale group j / 2
-              const uint32_t sw = (j >> 1) ? sc.y : sc.x;
-              const uint32_t s_lo = __byte_perm(sw, sw, 0x1010);   // {s[g], s[g]}
-              const uint32_t s_hi = __byte_perm(sw, sw, 0x3232);   // {s[g+8], s[g+8]}
-              uint32_t d[4];
-              decode_word_offset136(w4[j], mask, magic, d);
-#pragma unroll
-              for (int r = 0; r < 4; ++r) {   // d[r]: fragment register a_r (rows g, g+8, g, g+8)
-                __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&d[r]);
-                x = __hsub2(x, k136);
-                const uint32_t sr = (r & 1) ? s_hi : s_lo;
-                x = __hmul2(x, *reinterpret_cast<const __nv_bfloat162*>(&sr));
-                v[sl][4 * j + r] = *reinterpret_cast<uint32_t*>(&x);
-              }
-            }
-          }
-        }
+        if (active) dequant_two_slabs(smem + sp * kPStageBytes, q_off, s_off, mask, magic, v);
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[sp]);     // packed data consumed into registers
         if (active) {
@@ -385,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mine = __uint_as_float(v[c]);
             const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
             if (!(lane & 8) && c < ncol) {
-              const float h = mine / (1.0f + __expf(-mine)) * other;
+              const float h = __fdividef(mine, 1.0f + __expf(-mine)) * other;
               a.C[static_cast<size_t>(item.row0 + c0 + c) * a.ldc + col] = f32_to_bf16_rn(h);
             }
           }
