@@ -5,9 +5,11 @@
 // persistent warp-specialised main loop pipelining TMA loads, dequantisation
 // and the MMA.  Design on sm_103a (one CTA per SM, persistent):
 //   * work item = (local expert, 128 weight rows, pass of up to 192 of the
-//     expert's rows); items are dealt round-robin to the CTAs, so the CTAs
-//     running at one time cover a few experts and their activation rows
-//     stay in L2;
+//     expert's rows), numbered expert by expert; warp 0 takes the next
+//     number from a global counter (items differ in rows, so a static deal
+//     leaves SMs idle) and passes it to the other roles through a small
+//     mbarrier ring; the CTAs running at one time cover a few experts, whose
+//     activation rows stay in L2; the last CTA to run dry zeroes the counter;
 //   * the MMA is "swap AB": the 128 weight rows are M, the expert's rows
 //     (tokens) are N (a multiple of 16 up to 192), so an expert's rows are
 //     padded to 16, not to 128;
@@ -60,6 +62,10 @@ constexpr int kDequantWarp0 = 4, kDequantWarps = 8;
 constexpr int kEpiWarp0 = kDequantWarp0 + kDequantWarps;   // 12: warp index % 4 = lane quarter
 constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kMaxExperts = 1024;
+constexpr int kItemSlots = 4;
+// roles that read each item from the ring: activation producer, MMA warp,
+// dequant warps, epilogue warps
+constexpr int kItemReaders = 1 + 1 + kDequantWarps + 4;
 static_assert(kSmemBytes + (kMaxExperts + 1) * 4 + 512 <= 232448, "shared memory budget");
 static_assert((kBHalfBytes % 1024) == 0 && (kPOff % 1024) == 0, "SW128 tiles");
 static_assert((kDequantWarp0 % 4) == 0 && (kEpiWarp0 % 4) == 0, "warp index selects the TMEM lane quarter");
@@ -68,6 +74,7 @@ struct LargeArgs {
   const uint8_t* packed;
   const int32_t* counts;
   const int32_t* offsets;
+  int* work;        // [0] next item, [1] CTAs done; zero before the launch, zero after it
   uint16_t* C;
   int* status;
   int N, K, ldc, E_local, n_blob_tiles;
@@ -161,6 +168,19 @@ __device__ __forceinline__ void dequant_two_slabs(const uint8_t* pst, const uint
   }
 }
 
+// Next item from the CTA's item ring (consumer q of this role): the global
+// item number, -1 at the end of the work, -2 on a timeout.  All lanes of the
+// calling warp wait; lane 0 releases the slot.
+__device__ __forceinline__ int take_item(uint64_t* item_full, uint64_t* item_empty, const volatile int* item_q,
+                                         int q, int* status) {
+  const int slot = q % kItemSlots;
+  if (!mbar_wait(&item_full[slot], (q / kItemSlots) & 1, status)) return -2;
+  const int i = item_q[slot];
+  __syncwarp(__activemask());
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&item_empty[slot]);
+  return i;
+}
+
 // 64-wide K units in stage ks (the last stage of a K that is an odd number
 // of units holds one).
 __device__ __forceinline__ int stage_units(int ks, int n_units) {
@@ -175,6 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t b_full[kSB], b_empty[kSB];
   __shared__ __align__(8) uint64_t a_full[kSA], a_empty[kSA];
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], done_bar;
+  __shared__ __align__(8) uint64_t item_full[kItemSlots], item_empty[kItemSlots];
+  __shared__ volatile int item_q[kItemSlots];
   __shared__ uint32_t tmem_base_s;
   __shared__ int prefix[kMaxExperts + 1];
   __shared__ int hdr_ok;
@@ -209,6 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty_bar[b], 4);
     }
     mbar_init(&done_bar, 1);
+    for (int q = 0; q < kItemSlots; ++q) {
+      mbar_init(&item_full[q], 1);
+      mbar_init(&item_empty[q], kItemReaders);
+    }
     fence_mbar_init();
   }
   // the item prefix over experts
@@ -241,7 +267,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ packed-weight producer
     if (lane == 0) {
       int it = 0;
-      for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x) {
+      bool ok = true;
+      for (int q = 0;; ++q) {
+        int i = atomicAdd(a.work, 1);
+        if (i >= total_items || abort_flag) i = -1;
+        const int slot = q % kItemSlots;
+        if (q >= kItemSlots && !mbar_wait_backoff(&item_empty[slot], ((q / kItemSlots) - 1) & 1, a.status)) {
+          abort_flag = 1;
+          ok = false;
+          break;
+        }
+        item_q[slot] = i;
+        mbar_arrive(&item_full[slot]);   // release: the item number is visible to the waiters
+        if (i < 0) break;
         const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
         const uint8_t* t0 = a.packed + kPackHeaderBytes +
                             (static_cast<size_t>(item.e) * a.n_blob_tiles + 2 * item.wt) *
@@ -260,6 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_g2s(dst + kStageUnits * kUnitBytes, t0 + a.tile_bytes + src, bytes, &p_full[s]);
         }
       }
+      // the last CTA to run out of items zeroes the counters for the next launch
+      if (ok && atomicAdd(a.work + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        atomicExch(a.work, 0);
+        atomicExch(a.work + 1, 0);
+      }
       // drain: every issued copy must land before the CTA can exit
       for (int j = max(0, it - kSP); j < it; ++j)
         mbar_wait(&p_full[j % kSP], (j / kSP) & 1, a.status);
@@ -268,7 +311,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------- activation producer
     if (lane == 0) {
       int it = 0;
-      for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x) {
+      for (int q = 0; !abort_flag; ++q) {
+        const int i = take_item(item_full, item_empty, item_q, q, a.status);
+        if (i < 0) {
+          if (i == -2) abort_flag = 1;
+          break;
+        }
         const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
         const int n_mma = (item.rows + 15) & ~15;
         const bool small = n_mma <= a.box_s;
@@ -300,7 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       int it = 0, j = 0;
       bool issued_any = false;
-      for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x, ++j) {
+      for (; !abort_flag; ++j) {
+        int i = take_item(item_full, item_empty, item_q, j, a.status);
+        i = __shfl_sync(0xffffffffu, i, 0);   // warp-uniform before elect.sync
+        if (i < 0) {
+          if (i == -2) abort_flag = 1;
+          break;
+        }
         const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
         const int acc = j & 1, use = j >> 1;
         if (use >= 1 && !mbar_wait(&tempty_bar[acc], (use - 1) & 1, a.status)) {
@@ -365,7 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
     int it = 0;
-    for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x) {
+    for (int q = 0; !abort_flag; ++q) {
+      int i = take_item(item_full, item_empty, item_q, q, a.status);
+      i = __shfl_sync(0xffffffffu, i, 0);
+      if (i < 0) {
+        if (i == -2) abort_flag = 1;
+        break;
+      }
       for (int ks = 0; ks < n_stages; ++ks, ++it) {
         const int sp = it % kSP, sa = it % kSA;
         bool ok = mbar_wait(&p_full[sp], (it / kSP) & 1, a.status) &&
@@ -396,7 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int qw = warp & 3;                 // TMEM lane quarter of this warp
     int j = 0;
-    for (int i = blockIdx.x; i < total_items && !abort_flag; i += gridDim.x, ++j) {
+    for (; !abort_flag; ++j) {
+      int i = take_item(item_full, item_empty, item_q, j, a.status);
+      i = __shfl_sync(0xffffffffu, i, 0);
+      if (i < 0) {
+        if (i == -2) abort_flag = 1;
+        break;
+      }
       const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
       const int acc = j & 1, use = j >> 1;
       if (!mbar_wait_backoff(&tfull_bar[acc], use & 1, a.status)) {
@@ -505,6 +571,7 @@ cudaError_t gemm_large_launch(const GemmLaunch& g, const uint16_t* B, size_t b_r
   a.packed = static_cast<const uint8_t*>(g.packed);
   a.counts = g.counts;
   a.offsets = g.offsets;
+  a.work = g.work;
   a.C = g.C;
   a.status = g.status;
   a.N = g.N;
