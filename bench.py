@@ -64,6 +64,9 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--cpu-budget-s", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--report", choices=["route_align", "m_sweep"], default=None,
+                   help="report-only measurements instead of the headline line: router+align "
+                        "microseconds per (M, BLOCK_M), or the layer over M = 1..8192 at EP8 shapes")
     return p.parse_args()
 
 
@@ -491,8 +494,112 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def graph_us(fns, reps_in_graph=20, replays=30):
+    """Median microseconds of one pass of fns, from a CUDA graph holding
+    reps_in_graph passes, replayed between CUDA events on the launching stream."""
+    import torch
+    for f in fns:
+        f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps_in_graph):
+            for f in fns:
+                f()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1000.0 / reps_in_graph)
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def run_report(args):
+    """Report-only curves (one JSON line): router+align latency per (M,
+    BLOCK_M) over 384 experts, or the whole layer over M at EP8 shapes."""
+    import torch
+    from w4a16_int4_weight_sigmoid_gb300 import build as B
+    from w4a16_int4_weight_sigmoid_gb300 import chord
+    from w4a16_int4_weight_sigmoid_gb300 import workload as wl
+    from w4a16_int4_weight_sigmoid_gb300.layer import W4A16MoELayer, to_device
+    B.build()
+    chord.lib()
+    dev = "cuda:0"
+    rows = []
+    if args.report == "route_align":
+        E, k = wl.ROUTER_ALIGN_E, wl.ROUTER_ALIGN_TOPK
+        for M in wl.ROUTER_ALIGN_M:
+            logits, bias = wl.router_inputs(M, E, wl.ROUTER_ALIGN_SEED)
+            lg, bs = to_device(logits, dev), to_device(bias, dev)
+            tw = torch.empty((M, k), dtype=torch.float32, device=dev)
+            ti = torch.empty((M, k), dtype=torch.int32, device=dev)
+            route = lambda: chord.chord_moe_route(lg, bs, k, tw, ti)
+            t_route = graph_us([route])
+            for bm in wl.ROUTER_ALIGN_BM:
+                cap = chord.chord_moe_align_capacity(M, k, E, bm)
+                i32 = torch.int32
+                st = torch.empty(cap, dtype=i32, device=dev)
+                eid = torch.empty(cap // bm, dtype=i32, device=dev)
+                ntpp = torch.empty(1, dtype=i32, device=dev)
+                cnt = torch.empty(E, dtype=i32, device=dev)
+                off = torch.empty(E + 1, dtype=i32, device=dev)
+                pos = torch.empty(M * k, dtype=i32, device=dev)
+                wsb = chord.chord_moe_align_workspace_bytes(M, k, E)
+                aws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
+                align = lambda: chord.chord_moe_align(ti, 0, E, bm, st, eid, ntpp, cnt, off, pos, aws)
+                fused = lambda: chord.chord_moe_route_align(lg, bs, k, 0, E, bm, tw, ti, st, eid, ntpp, cnt,
+                                                            off, pos, aws)
+                rows.append({"M": M, "block_m": bm, "route_us": round(t_route, 2),
+                             "align_us": round(graph_us([align]), 2),
+                             "route_then_align_us": round(graph_us([route, align]), 2),
+                             "chord_moe_route_align_us": round(graph_us([fused]), 2)})
+        note = "CUDA graph of 20 back-to-back passes, median of 30 replays; 384 experts, top-8, all local"
+    else:
+        base = wl.EP8_DECODE
+        d = wl.layer_inputs(wl.LayerShape("m_sweep", 8192, base.H, base.I, base.E_total, base.E_local,
+                                          0, base.topk, base.seed))
+        layer = W4A16MoELayer(d["w13_q"], d["w13_s"], d["w2_q"], d["w2_s"], base.E_total, 0, base.topk,
+                              device=dev)
+        x, lg, bs = to_device(d["x"], dev), to_device(d["logits"], dev), to_device(d["bias"], dev)
+        del d
+        M = 1
+        while M <= 8192:
+            xm, lm = x[:M].contiguous(), lg[:M].contiguous()
+            out = torch.empty((M, base.H), dtype=torch.bfloat16, device=dev)
+            layer.workspace(M)
+            n_in = 5 if M >= 1024 else 20
+            fwd = lambda: layer.forward(xm, lm, bs, out=out)
+            us = graph_us([fwd], reps_in_graph=n_in, replays=10)
+            plan = chord.chord_moe_layer_plan(M, base.E_total, base.topk)
+            row = {"M": M, "us": round(us, 2), "tokens_per_s": round(M / (us * 1e-6), 1),
+                   "path": "tcgen05" if plan.path == chord.CHORD_PATH_LARGE_M else "register-mma",
+                   "rows_per_pass": plan.rows_per_pass}
+            for name, pth in (("us_register_mma", chord.CHORD_PATH_SMALL_M),
+                              ("us_tcgen05", chord.CHORD_PATH_LARGE_M)):
+                tun = chord.chord_tuning(pth, 0, 0, 0)
+                f2 = lambda: layer.forward(xm, lm, bs, out=out, tuning=tun)
+                row[name] = round(graph_us([f2], reps_in_graph=n_in, replays=10), 2)
+            rows.append(row)
+            M *= 2
+        note = ("one layer, chord_moe_layer, EP8 shapes (H 7168, I 2048, 48 of 384 experts, top-8), "
+                "the first M tokens of one seeded 8192-token draw; CUDA graph of back-to-back calls")
+    if torch.cuda.is_available():
+        assert int(layer.dev_status.item() if args.report == "m_sweep" else 0) == 0
+    print(json.dumps({"report": args.report, "unit": "us", "note": note, "rows": rows}))
+
+
 def main():
     args = parse_args()
+    if args.report:
+        run_report(args)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -134,6 +134,27 @@ int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, 
                     int32_t* expert_offsets, int32_t* sorted_positions, void* workspace,
                     size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------- route + align
+ * chord_moe_route followed by chord_moe_align in one call, with their
+ * arguments and bit-identical outputs ([Router] "코드 분석" and "커널 내부
+ * 로직 변경": the fused router kernel also produces the align buffers and
+ * re-initialises its counters at entry).  For M <= 16 tokens it is one
+ * launch of one CTA (one warp routes each token, block barrier, one-chunk
+ * stable counting sort), which saves a launch and a round trip through the
+ * topk_ids buffer; larger calls run the two kernels, whose router grid
+ * spreads the tokens over many CTAs.
+ *   logits, bias, E_total, topk, topk_weights, topk_ids   as chord_moe_route
+ *   expert_begin .. sorted_positions, workspace, ws_bytes as chord_moe_align
+ *                  (the workspace is needed only when M*topk > 4096)
+ * Errors as the two calls; local experts must lie within [0, E_total).
+ */
+int chord_moe_route_align(const float* logits, const float* bias, int M, int E_total, int topk,
+                          int expert_begin, int E_local, int block_m, size_t capacity,
+                          float* topk_weights, int32_t* topk_ids, int32_t* sorted_token_ids,
+                          int32_t* expert_ids, int32_t* num_tokens_post_padded, int32_t* expert_counts,
+                          int32_t* expert_offsets, int32_t* sorted_positions, void* workspace,
+                          size_t ws_bytes, void* stream);
+
 /* Allocation-free variant of chord_moe_align.  The pages have no counterpart;
  * it exists for callers that cannot allocate device memory at all: code
  * running under an engine or plugin that owns every device allocation and
@@ -245,7 +266,9 @@ int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t*
 size_t chord_moe_layer_workspace_bytes(int M, int H, int I, int E_local, int topk);
 /* Host-only: the tuning chord_moe_layer uses for these shapes (tokens-per-
  * expert policy, [Chord] "인덱스 커널 기법": the schedule follows the tokens
- * delivered per expert, tok_e = M*topk/E_total).  Writes *plan; returns
+ * delivered per expert, tok_e = M*topk/E_total; the tcgen05 path from
+ * tok_e >= 10, where the two paths measured even on GB300, the register-MMA
+ * path below it with 8 or 16 rows per pass).  Writes *plan; returns
  * CHORD_OK or CHORD_ERR_INVALID_ARG.  Passing the plan to
  * chord_w4a16_moe_gemm reproduces the layer's launches exactly. */
 int chord_moe_layer_plan(int M, int E_total, int topk, chord_tuning* plan);

@@ -141,3 +141,62 @@ def test_align_all_dropped_and_empty():
     got = gpu_align(np.zeros((0, 8), np.int32), 0, 384, 16)
     assert got["num_tokens_post_padded"] == 0 and np.all(got["expert_counts"] == 0)
     assert np.all(got["expert_offsets"] == 0)
+
+
+# ------------------------------------------------------- fused route + align
+def gpu_route_align(logits, bias, k, begin, E_local, bm):
+    M, E = logits.shape
+    dev = "cuda"
+    cap = chord.chord_moe_align_capacity(M, k, E_local, bm)
+    lg, bs = torch.from_numpy(logits).to(dev), torch.from_numpy(bias).to(dev)
+    w = torch.full((M, k), -1.0, dtype=torch.float32, device=dev)
+    ids = torch.full((M, k), -1, dtype=torch.int32, device=dev)
+    st = torch.full((max(cap, 1),), -7, dtype=torch.int32, device=dev)
+    eid = torch.full((max(cap // bm, 1),), -7, dtype=torch.int32, device=dev)
+    ntpp = torch.full((1,), -7, dtype=torch.int32, device=dev)
+    cnt = torch.full((E_local,), -7, dtype=torch.int32, device=dev)
+    off = torch.full((E_local + 1,), -7, dtype=torch.int32, device=dev)
+    pos = torch.full((max(M * k, 1),), -7, dtype=torch.int32, device=dev)
+    wsb = chord.chord_moe_align_workspace_bytes(M, k, E_local)
+    ws = torch.full((max(wsb, 16),), 0x5A, dtype=torch.uint8, device=dev) if wsb else None
+    chord.chord_moe_route_align(lg, bs, k, begin, E_local, bm, w, ids, st[:cap] if cap else st, eid, ntpp,
+                                cnt, off, pos, ws)
+    torch.cuda.synchronize()
+    n = int(ntpp.item())
+    return w.cpu().numpy(), ids.cpu().numpy(), dict(
+        sorted_token_ids=st.cpu().numpy()[:n], expert_ids=eid.cpu().numpy()[:n // bm],
+        num_tokens_post_padded=n, expert_counts=cnt.cpu().numpy(), expert_offsets=off.cpu().numpy(),
+        sorted_positions=pos.cpu().numpy()[:M * k])
+
+
+def check_route_align(logits, bias, k, begin, E_local, bm):
+    rw, rids, _ = oracle.route(logits, bias, k)
+    ref = oracle.moe_align(rids, begin, E_local, bm)
+    for _ in range(2):
+        w, ids, got = gpu_route_align(logits, bias, k, begin, E_local, bm)
+        assert np.array_equal(ids, rids)
+        assert np.array_equal(w.view(np.uint32), rw.view(np.uint32))
+        assert got["num_tokens_post_padded"] == ref["num_tokens_post_padded"]
+        for key in ("expert_counts", "expert_offsets", "sorted_token_ids", "expert_ids", "sorted_positions"):
+            assert np.array_equal(got[key], ref[key]), key
+
+
+@pytest.mark.parametrize("M", wl.ROUTER_ALIGN_M)
+@pytest.mark.parametrize("bm", wl.ROUTER_ALIGN_BM)
+def test_route_align_fused_router_workload(M, bm):
+    """One launch up to 16 tokens (M = 1, 8); larger M takes the two-launch path."""
+    logits, bias = wl.router_inputs(M, wl.ROUTER_ALIGN_E, wl.ROUTER_ALIGN_SEED)
+    check_route_align(logits, bias, wl.ROUTER_ALIGN_TOPK, 0, wl.ROUTER_ALIGN_E, bm)
+
+
+@pytest.mark.parametrize("M,E,k,begin,E_local,bm", [
+    (16, 384, 8, 96, 48, 16),        # the largest one-launch batch, shard in the middle
+    (17, 384, 8, 0, 48, 8),          # one token more: two launches
+    (16, 1024, 32, 0, 1024, 128),    # widest router and shard in one launch
+    (7, 1, 1, 0, 1, 128),
+    (9, 1000, 17, 500, 500, 64),
+    (0, 384, 8, 0, 48, 16),
+])
+def test_route_align_fused_edges(M, E, k, begin, E_local, bm):
+    logits, bias = wl.router_inputs(M, E, 41)
+    check_route_align(logits, bias, k, begin, E_local, bm)

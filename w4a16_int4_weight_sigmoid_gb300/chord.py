@@ -54,6 +54,8 @@ _SIGS = {
     "chord_moe_align_workspace_bytes": (_Z, [_I, _I, _I]),
     "chord_moe_align": (_I, [_P, _I, _I, _I, _I, _I, _Z, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "chord_moe_align_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _Z, _P, _P, _P, _P, _P, _P, _P]),
+    "chord_moe_route_align": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _Z, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _P, _Z, _P]),
     "chord_w4a16_prepack_bytes": (_Z, [_I, _I, _I, _I]),
     "chord_w4a16_prepack": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "chord_w4a16_moe_gemm_workspace_bytes": (_Z, [_Z, _I, _I]),
@@ -150,6 +152,24 @@ def chord_moe_align(topk_ids, expert_begin: int, E_local: int, block_m: int, sor
         _ptr(expert_counts, i32, "expert_counts"), _ptr(expert_offsets, i32, "expert_offsets"),
         _ptr(sorted_positions, i32, "sorted_positions"), _ptr(workspace, None, "workspace"),
         ws_bytes, _stream(stream)))
+
+
+def chord_moe_route_align(logits, bias, topk: int, expert_begin: int, E_local: int, block_m: int,
+                          topk_weights, topk_ids, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                          expert_counts, expert_offsets, sorted_positions=None, workspace=None,
+                          stream=None):
+    """chord_moe_route then chord_moe_align in one call (one launch for M <= 16)."""
+    M, E_total = logits.shape
+    i32 = torch.int32
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().chord_moe_route_align(
+        _ptr(logits, torch.float32, "logits"), _ptr(bias, torch.float32, "bias"), M, E_total, topk,
+        expert_begin, E_local, block_m, sorted_token_ids.numel(),
+        _ptr(topk_weights, torch.float32, "topk_weights"), _ptr(topk_ids, i32, "topk_ids"),
+        _ptr(sorted_token_ids, i32, "sorted_token_ids"), _ptr(expert_ids, i32, "expert_ids"),
+        _ptr(num_tokens_post_padded, i32, "ntpp"), _ptr(expert_counts, i32, "expert_counts"),
+        _ptr(expert_offsets, i32, "expert_offsets"), _ptr(sorted_positions, i32, "sorted_positions"),
+        _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)))
 
 
 def chord_moe_align_noalloc(topk_ids, expert_begin: int, E_local: int, block_m: int,

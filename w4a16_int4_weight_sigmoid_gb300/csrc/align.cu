@@ -1,174 +1,14 @@
-// moe_align_block_size: stable counting sort of token->expert assignments.
-//
-// Buffers: [Router] "코드 분석" arg_plan (sorted_token_ids, expert_ids,
-// num_tokens_post_padded, expert_counts, expert_offsets; the per-expert
-// scatter cursors are re-initialised on entry as in "커널 내부 로직 변경").
-//
-// Each CTA owns a chunk of 4096 consecutive assignments; each of its 16
-// warps owns 256 consecutive ones, walked in 8 steps of 32.  Within a step,
-// __match_any_sync groups lanes with the same expert, the lowest lane of the
-// group advances the warp's counter for that expert, and each lane's rank is
-// the counter's old value plus the number of earlier lanes in its group.  An
-// exclusive prefix over warps then turns per-warp ranks into chunk ranks that
-// preserve the flat-index order.  One chunk: one launch does everything.
-// More chunks: phase 1 writes chunk ranks and per-chunk counts to the
-// workspace, phase 2 adds the prefix over chunks and scatters.
+// moe_align_block_size: stable counting sort of token->expert assignments
+// (device code in align_impl.cuh).  One chunk of up to 4096 assignments: one
+// launch does everything.  More chunks: phase 1 writes chunk ranks and
+// per-chunk counts to the workspace, phase 2 adds the prefix over chunks and
+// scatters.
 #include "common.cuh"
 #include "kernels.h"
+#include "align_impl.cuh"
 
 namespace chord {
 namespace {
-
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kPerThread = 8;
-constexpr int kChunk = kThreads * kPerThread;  // 4096 assignments per CTA
-
-struct AlignArgs {
-  const int32_t* ids;
-  int n, sentinel, begin, E, bm;
-  int32_t *sorted, *expert_ids, *ntpp, *counts, *offsets, *positions;
-  int32_t *ws_rank, *ws_counts;  // multi-chunk only
-  int G;
-};
-
-// smem layout (ints): wcnt[kWarps][E] | tot[E] | base[E] | off[E+1]
-__device__ __forceinline__ int* sm_wcnt(int* s) { return s; }
-__device__ __forceinline__ int* sm_tot(int* s, int E) { return s + kWarps * E; }
-__device__ __forceinline__ int* sm_base(int* s, int E) { return s + (kWarps + 1) * E; }
-__device__ __forceinline__ int* sm_off(int* s, int E) { return s + (kWarps + 2) * E; }
-
-__device__ __forceinline__ int elem_index(int g, int warp, int step, int lane) {
-  return g * kChunk + warp * (32 * kPerThread) + step * 32 + lane;
-}
-
-// Per-chunk stable ranks; loc[] = local expert or -1; tot[e] = chunk count.
-__device__ void chunk_rank(const AlignArgs& a, int g, int* s, int (&loc)[kPerThread],
-                           int (&rank)[kPerThread]) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int E = a.E;
-  int* wcnt = sm_wcnt(s);
-  for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
-  __syncthreads();
-  const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-  for (int step = 0; step < kPerThread; ++step) {
-    const int idx = elem_index(g, warp, step, lane);
-    int e = -1;
-    if (idx < a.n) {
-      e = a.ids[idx] - a.begin;
-      if (e < 0 || e >= E) e = -1;
-    }
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    const int leader = __ffs(peers) - 1;
-    int base = 0;
-    if (e >= 0 && lane == leader) {
-      base = wcnt[warp * E + e];
-      wcnt[warp * E + e] = base + __popc(peers);
-    }
-    base = __shfl_sync(0xffffffffu, base, leader);
-    loc[step] = e;
-    rank[step] = base + __popc(peers & lt);
-  }
-  __syncthreads();
-  int* tot = sm_tot(s, E);
-  for (int e = tid; e < E; e += kThreads) {
-    int run = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      const int c = wcnt[w * E + e];
-      wcnt[w * E + e] = run;
-      run += c;
-    }
-    tot[e] = run;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int step = 0; step < kPerThread; ++step)
-    if (loc[step] >= 0) rank[step] += wcnt[warp * E + loc[step]];
-}
-
-// Exclusive scan of in[0..n) into out[0..n] (out[n] = total); n <= 2*kThreads.
-__device__ void block_exclusive_scan(const int* in, int* out, int n, int* scratch /*kWarps+1*/) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i0 = 2 * tid;
-  const int v0 = i0 < n ? in[i0] : 0;
-  const int v1 = i0 + 1 < n ? in[i0 + 1] : 0;
-  int sum = v0 + v1, inc = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += t;
-  }
-  if (lane == 31) scratch[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kWarps ? scratch[lane] : 0, wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += t;
-    }
-    if (lane < kWarps) scratch[lane] = wi - w;  // exclusive warp offsets
-    if (lane == kWarps - 1) scratch[kWarps] = wi;
-  }
-  __syncthreads();
-  const int ex = scratch[warp] + inc - sum;
-  if (i0 < n) out[i0] = ex;
-  if (i0 + 1 < n) out[i0 + 1] = ex + v0;
-  if (tid == 0) out[n] = scratch[kWarps];
-  __syncthreads();
-}
-
-// Given tot (all-chunk counts) and base (this chunk's start per expert):
-// offsets, scatter, metadata.
-__device__ void scatter_chunk(const AlignArgs& a, int g, int* s, const int (&loc)[kPerThread],
-                              const int (&rank)[kPerThread], int* scan_scratch) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int E = a.E, bm = a.bm;
-  int* tot = sm_tot(s, E);
-  int* base = sm_base(s, E);
-  int* off = sm_off(s, E);
-  // padded counts into wcnt's space (no longer needed), then scan into off
-  int* pad = sm_wcnt(s);
-  for (int e = tid; e < E; e += kThreads) pad[e] = (tot[e] + bm - 1) / bm * bm;
-  __syncthreads();
-  block_exclusive_scan(pad, off, E, scan_scratch);
-#pragma unroll
-  for (int step = 0; step < kPerThread; ++step) {
-    const int idx = elem_index(g, warp, step, lane);
-    if (idx >= a.n) continue;
-    const int e = loc[step];
-    if (e >= 0) {
-      const int pos = off[e] + base[e] + rank[step];
-      a.sorted[pos] = idx;
-      if (a.positions) a.positions[idx] = pos;
-    } else if (a.positions) {
-      a.positions[idx] = -1;
-    }
-  }
-  // metadata, spread over the chunks' CTAs
-  for (int e = tid; e < E; e += kThreads) {
-    if (e % a.G != g) continue;
-    a.counts[e] = tot[e];
-    a.offsets[e] = off[e];
-    for (int p = off[e] + tot[e]; p < off[e + 1]; ++p) a.sorted[p] = a.sentinel;
-  }
-  const int total = off[E];
-  const int nblk = total / bm;
-  for (int b = g * kThreads + tid; b < nblk; b += a.G * kThreads) {
-    const int row = b * bm;
-    int lo = 0, hi = E - 1;  // largest e with off[e] <= row
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (off[mid] <= row) lo = mid; else hi = mid - 1;
-    }
-    a.expert_ids[b] = lo;
-  }
-  if (g == 0 && tid == 0) {
-    a.offsets[E] = total;
-    a.ntpp[0] = total;
-  }
-}
 
 __global__ void __launch_bounds__(kThreads) align_single_kernel(AlignArgs a) {
   extern __shared__ int s[];
@@ -231,7 +71,6 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(AlignArgs a) {
   scatter_chunk(a, g, s, loc, rank, scan_scratch);
 }
 
-size_t align_smem_bytes(int E) { return static_cast<size_t>((kWarps + 3) * E + 1) * sizeof(int); }
 
 }  // namespace
 

@@ -51,10 +51,17 @@ int rows_per_pass_for(double tok_e) {
   return 32;
 }
 
-// Expected rows per expert at or above which the tensor-core (tcgen05) path
-// is used; [Chord] "인덱스 커널 기법" switches schedules around 80 rows per
-// expert.
+// chord_w4a16_moe_gemm's automatic path: expected rows per local expert,
+// counting every assignment as local (the call does not know E_total), at
+// or above which the tensor-core (tcgen05) path is used; [Chord] "인덱스 커널
+// 기법" switches schedules around 80 rows per expert.
 constexpr double kLargeTokE = 64.0;
+// chord_moe_layer's policy: expected rows per expert M*topk/E_total at or
+// above which the tcgen05 path is used.  Measured on GB300 at Kimi EP8
+// shapes (whole layer, both paths forced): M = 256 -> register path 288 us
+// vs 397 us; M = 512 -> 439 vs 434 us; M = 1024 -> 936 vs 464 us, so the
+// paths cross at about 10 rows per expert.
+constexpr double kLayerLargeTokE = 10.0;
 constexpr size_t kWorkBytes = 256;   // work-queue counters at the start of a GEMM workspace
 
 // BLOCK_M the layer aligns with: one small-M pass per block, or 16 (the
@@ -175,6 +182,42 @@ int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, 
                                       expert_counts, expert_offsets, sorted_positions, workspace,
                                       static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "align launch");
+}
+
+int chord_moe_route_align(const float* logits, const float* bias, int M, int E_total, int topk,
+                          int expert_begin, int E_local, int block_m, size_t capacity,
+                          float* topk_weights, int32_t* topk_ids, int32_t* sorted_token_ids,
+                          int32_t* expert_ids, int32_t* num_tokens_post_padded, int32_t* expert_counts,
+                          int32_t* expert_offsets, int32_t* sorted_positions, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  if (M < 0) return fail(CHORD_ERR_INVALID_ARG, "M=%d < 0", M);
+  if (E_total < 1 || E_total > 1024) return fail(CHORD_ERR_INVALID_ARG, "E_total=%d not in [1, 1024]", E_total);
+  if (topk < 1 || topk > E_total || topk > 32)
+    return fail(CHORD_ERR_INVALID_ARG, "topk=%d not in [1, min(E_total, 32)]", topk);
+  if (E_local < 1 || E_local > 1024) return fail(CHORD_ERR_INVALID_ARG, "E_local=%d not in [1, 1024]", E_local);
+  if (expert_begin < 0 || expert_begin + E_local > E_total)
+    return fail(CHORD_ERR_INVALID_ARG, "local experts [%d, %d) not within E_total=%d", expert_begin,
+                expert_begin + E_local, E_total);
+  if (!valid_block_m(block_m)) return fail(CHORD_ERR_INVALID_ARG, "block_m=%d not in {8,16,32,64,128}", block_m);
+  const size_t need = chord_moe_align_capacity(M, topk, E_local, block_m);
+  if (capacity < need) return fail(CHORD_ERR_INVALID_ARG, "capacity %zu < required %zu", capacity, need);
+  if (!expert_ids || !num_tokens_post_padded || !expert_counts || !expert_offsets || !sorted_token_ids ||
+      (M > 0 && (!logits || !bias || !topk_weights || !topk_ids)))
+    return fail(CHORD_ERR_INVALID_ARG, "null pointer");
+  const long long n = static_cast<long long>(M) * topk;
+  if (!chord::route_align_fits(M, n, E_local)) {
+    // more than one chunk: the two separate launches
+    int rc = chord_moe_route(logits, bias, M, E_total, topk, topk_weights, topk_ids, stream);
+    if (rc) return rc;
+    return chord_moe_align(topk_ids, M, topk, expert_begin, E_local, block_m, capacity, sorted_token_ids,
+                           expert_ids, num_tokens_post_padded, expert_counts, expert_offsets,
+                           sorted_positions, workspace, ws_bytes, stream);
+  }
+  cudaError_t e = chord::route_align_launch(logits, bias, M, E_total, topk, expert_begin, E_local, block_m,
+                                            topk_weights, topk_ids, sorted_token_ids, expert_ids,
+                                            num_tokens_post_padded, expert_counts, expert_offsets,
+                                            sorted_positions, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "route+align launch");
 }
 
 int chord_moe_align_noalloc(const int32_t* topk_ids, int M, int topk, int expert_begin, int E_local,
@@ -315,7 +358,7 @@ int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t*
 int chord_moe_layer_plan(int M, int E_total, int topk, chord_tuning* plan) {
   if (!plan || M < 0 || E_total < 1 || topk < 1) return fail(CHORD_ERR_INVALID_ARG, "bad plan arguments");
   const double tok_e = static_cast<double>(M) * topk / E_total;
-  plan->path = tok_e >= kLargeTokE ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
+  plan->path = tok_e >= kLayerLargeTokE ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
   plan->rows_per_pass = rows_per_pass_for(tok_e);
   plan->use_f16_accum = 0;
   plan->batch_invariant = 0;
@@ -372,10 +415,10 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
 
   cudaError_t ce = cudaMemsetAsync(ws + w.work, 0, 2 * kWorkBytes, st);
   if (ce != cudaSuccess) return cuda_fail(ce, "work counter reset");
-  rc = chord_moe_route(logits, bias, M, E_total, topk, tw, ids, stream);
-  if (rc) return rc;
-  rc = chord_moe_align(ids, M, topk, expert_begin, E_local, w.bm, w.cap, sorted, eids, ntpp, counts,
-                       offsets, pos, aws, chord_moe_align_workspace_bytes(M, topk, E_local), stream);
+  // one launch when the assignments fit one align chunk, else two
+  rc = chord_moe_route_align(logits, bias, M, E_total, topk, expert_begin, E_local, w.bm, w.cap, tw, ids,
+                             sorted, eids, ntpp, counts, offsets, pos, aws,
+                             chord_moe_align_workspace_bytes(M, topk, E_local), stream);
   if (rc) return rc;
   const double tok_e = static_cast<double>(M) * topk / E_total;
   rc = gemm_impl(x, 1, w13_packed, E_local, 2 * I, H, M, topk, sorted, eids, ntpp, counts, offsets,

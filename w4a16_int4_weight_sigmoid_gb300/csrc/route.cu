@@ -1,114 +1,22 @@
-// Sigmoid + bias top-k router: one warp per token, shuffle-based selection.
-//
-// Buffers: [Router] "코드 분석" (arg_plan: logits, bias, topk_weights,
-// topk_ids).  The sigmoid is the fixed binary32 op sequence documented in
-// chord_moe.h, written with explicitly rounded intrinsics (no contraction
-// into FMA), so every implementation of the sequence returns the same bits.
+// Sigmoid + bias top-k router: one warp per token, shuffle-based selection
+// (the per-token code is in route_impl.cuh).
 #include <cfloat>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "route_impl.cuh"
 
 namespace chord {
 namespace {
-
-// Constants derived from the mathematics: log2(e); ln 2 split into a head
-// with 16 fractional bits (n * head is exact for |n| <= 126) and a tail;
-// Taylor coefficients 1/j!.
-__device__ __forceinline__ float sigmoid_spec(float x) {
-  const float kLog2e = (float)(1.0 / 0.6931471805599453);
-  const float kLn2Hi = 45426.0f / 65536.0f;
-  const float kLn2Lo = (float)(0.6931471805599453 - 45426.0 / 65536.0);
-  const float c0 = 1.0f, c1 = 1.0f, c2 = (float)(1.0 / 2.0), c3 = (float)(1.0 / 6.0),
-              c4 = (float)(1.0 / 24.0), c5 = (float)(1.0 / 120.0), c6 = (float)(1.0 / 720.0),
-              c7 = (float)(1.0 / 5040.0);
-  float y = fminf(fmaxf(-x, -87.0f), 87.0f);
-  float n = rintf(__fmul_rn(y, kLog2e));
-  float r = __fsub_rn(y, __fmul_rn(n, kLn2Hi));
-  r = __fsub_rn(r, __fmul_rn(n, kLn2Lo));
-  float p = c7;
-  p = __fadd_rn(__fmul_rn(p, r), c6);
-  p = __fadd_rn(__fmul_rn(p, r), c5);
-  p = __fadd_rn(__fmul_rn(p, r), c4);
-  p = __fadd_rn(__fmul_rn(p, r), c3);
-  p = __fadd_rn(__fmul_rn(p, r), c2);
-  p = __fadd_rn(__fmul_rn(p, r), c1);
-  p = __fadd_rn(__fmul_rn(p, r), c0);
-  float e = __fmul_rn(p, __int_as_float((static_cast<int>(n) + 127) << 23));
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
-}
-
-// (key, id) as one integer whose order is the selection order: the key's
-// bits mapped to an order-preserving unsigned (keys are never -0.0: s > 0 and
-// s + b rounds x + (-x) to +0), then the complement of the id, so among equal
-// keys the smaller id compares larger.
-__device__ __forceinline__ uint64_t pack_key(float key, int id) {
-  const uint32_t b = __float_as_uint(key);
-  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return (static_cast<uint64_t>(ord) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(id));
-}
 
 template <int EPL>
 __global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ logits,
                                                     const float* __restrict__ bias, int M, int E,
                                                     int topk, float* __restrict__ w_out,
                                                     int32_t* __restrict__ id_out) {
-  const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= M) return;
-  const float* row = logits + static_cast<size_t>(t) * E;
-  // All loads first (clamped in-range addresses, no branches), so they are in
-  // flight together instead of one round trip per expert.
-  float lg[EPL], bs[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = min(lane + 32 * i, E - 1);
-    lg[i] = __ldg(row + e);
-    bs[i] = __ldg(bias + e);
-  }
-  uint64_t cand[EPL];
-  float sc[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    sc[i] = sigmoid_spec(lg[i]);
-    cand[i] = e < E ? pack_key(__fadd_rn(sc[i], bs[i]), e) : 0;  // 0: below every candidate
-  }
-  int my_id = 0;
-  float my_s = 0.f;
-  for (int r = 0; r < topk; ++r) {
-    uint64_t best = cand[0];
-#pragma unroll
-    for (int i = 1; i < EPL; ++i) best = cand[i] > best ? cand[i] : best;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-      best = o > best ? o : best;
-    }
-    const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
-    const int owner = id & 31, slot = id >> 5;
-    float s_mine = 0.f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      if (i == slot) {
-        s_mine = sc[i];
-        if (lane == owner) cand[i] = 0;
-      }
-    }
-    const float s_win = __shfl_sync(0xffffffffu, s_mine, owner);
-    if (lane == r) {
-      my_id = id;
-      my_s = s_win;
-    }
-  }
-  // S = s_0 + s_1 + ... in rank order, binary32.
-  float S = __shfl_sync(0xffffffffu, my_s, 0);
-  for (int r = 1; r < topk; ++r) S = __fadd_rn(S, __shfl_sync(0xffffffffu, my_s, r));
-  if (lane < topk) {
-    const size_t o = static_cast<size_t>(t) * topk + lane;
-    id_out[o] = my_id;
-    w_out[o] = __fdiv_rn(my_s, S);
-  }
+  route_token<EPL>(logits, bias, t, E, topk, w_out, id_out);
 }
 
 template <int EPL>
