@@ -238,6 +238,25 @@ int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w
                          size_t capacity, int epilogue, chord_bf16* C, const chord_tuning* tuning,
                          void* workspace, size_t ws_bytes, int* dev_status, void* stream);
 
+/* ------------------------------------------------------- dense W4A16 GEMM
+ * C = A * (q*s)^T for one weight matrix, no routing: the indexed GEMM above
+ * with every row belonging to a single expert ([Humming] "통합 양자화 표현":
+ * one weight format serves dense and MoE layers).  packed_w is a
+ * chord_w4a16_prepack blob with E = 1.
+ *   A          BF16 [M, K] (16-byte aligned)
+ *   C          BF16 [M, N] (STORE) or [M, N/2] (SILU_MUL)
+ *   workspace  chord_w4a16_gemm_workspace_bytes(M) bytes, 16-byte aligned;
+ *              zero it once when allocated (its first 256 bytes are
+ *              work-queue counters that every call leaves zero); each call
+ *              writes the one-expert block map into the rest on the device
+ * Path and rows per pass as chord_w4a16_moe_gemm with M rows per expert,
+ * unless tuning says otherwise.  Errors as chord_w4a16_moe_gemm.
+ */
+size_t chord_w4a16_gemm_workspace_bytes(int M);
+int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, int M, int epilogue,
+                     chord_bf16* C, const chord_tuning* tuning, void* workspace, size_t ws_bytes,
+                     int* dev_status, void* stream);
+
 /* --------------------------------------------------------- top-k weighted sum
  * moe_fused_mul_sum ([HumPR] "왜 이게 좋은가" 3: weight multiply and sum):
  *   out[t, :] = sum over j = 0..topk-1 with sorted_positions[t*topk+j] >= 0 of

@@ -151,3 +151,29 @@ def test_moe_sum_against_oracle():
     # FP32 sum of at most k products, one BF16 rounding
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
     assert np.all(got[np.all(al["sorted_positions"].reshape(M, k) < 0, axis=1)] == 0)
+
+
+@pytest.mark.parametrize("M,K,N,epi,path", [
+    (1, 256, 128, STORE, SMALL), (37, 512, 192, STORE, SMALL), (37, 512, 256, SILU, SMALL),
+    (100, 1024, 256, SILU, LARGE), (300, 256, 384, STORE, LARGE), (300, 256, 384, STORE, 0),
+    (5, 7168, 512, SILU, 0),
+])
+def test_dense_gemm(M, K, N, epi, path):
+    """Dense entry (E = 1, no routing) against the oracle's expert GEMM, twice per workspace."""
+    x = wl.activations(M, K, 51)
+    q = wl.int4_weights(1, N, K, 52, wl.S_Q13)
+    s = wl.group_scales(1, N, K, 53, wl.S_S13)
+    packed = prepack(to_device(q), to_device(s), epi == SILU)
+    acc = oracle.expert_rows_gemm(oracle.bf16_to_f64(x), oracle.dequant_expert(q[0], s[0]))
+    ref = oracle.silu_mul(acc) if epi == SILU else acc
+    ws = torch.zeros(chord.chord_w4a16_gemm_workspace_bytes(M), dtype=torch.uint8, device="cuda")
+    tun = chord.chord_tuning(path, 0, 0, 0)
+    for _ in range(2):
+        C = torch.full((M, N // 2 if epi == SILU else N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        chord.chord_w4a16_gemm(to_device(x), packed, N, K, epi, C, ws, tuning=tun, dev_status=status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        assert int(ws[:256].view(torch.int32).abs().sum().item()) == 0
+        tol = GEMM_TOL[LARGE] if path == LARGE or (path == 0 and M >= 64 and N % 128 == 0) else GEMM_TOL[SMALL]
+        assert_close_to_oracle(bf16_to_np(C), ref, "dense", *tol)

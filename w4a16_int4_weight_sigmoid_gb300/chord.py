@@ -62,6 +62,8 @@ _SIGS = {
     "chord_w4a16_moe_gemm": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _Z, _I,
                                   _P, _P, _P, _Z, _P, _P]),
     "chord_moe_sum": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "chord_w4a16_gemm_workspace_bytes": (_Z, [_I]),
+    "chord_w4a16_gemm": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P, _P]),
     "chord_moe_layer_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "chord_moe_layer_plan": (_I, [_I, _I, _I, _P]),
     "chord_moe_layer": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z,
@@ -217,6 +219,20 @@ def chord_w4a16_moe_gemm(A, a_gather: bool, packed_w, E_local: int, N: int, K: i
         _ptr(expert_counts, torch.int32, "expert_counts"),
         _ptr(expert_offsets, torch.int32, "expert_offsets"), block_m, sorted_token_ids.numel(),
         epilogue, _ptr(C, None, "C"), tun[0] if tun else None, _ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def chord_w4a16_gemm_workspace_bytes(M: int) -> int:
+    return lib().chord_w4a16_gemm_workspace_bytes(M)
+
+
+def chord_w4a16_gemm(A, packed_w, N: int, K: int, epilogue: int, C, workspace, tuning=None,
+                     dev_status=None, stream=None):
+    """Dense C = A (q*s)^T with a one-expert packed blob; workspace zeroed once when allocated."""
+    tun = _tuning(tuning)
+    _check(lib().chord_w4a16_gemm(
+        _ptr(A, None, "A"), _ptr(packed_w, torch.uint8, "packed_w"), N, K, A.shape[0], epilogue,
+        _ptr(C, None, "C"), tun[0] if tun else None, _ptr(workspace, torch.uint8, "workspace"),
         workspace.numel(), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 

@@ -345,6 +345,45 @@ int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w
                    C, tuning, tok_e, workspace, ws_bytes, dev_status, stream);
 }
 
+// [256 B work counters | counts, offsets, ntpp (256 B) | expert_ids]
+size_t chord_w4a16_gemm_workspace_bytes(int M) {
+  if (M < 0) return 0;
+  return 2 * kWorkBytes + round_up((static_cast<size_t>(M) / 8 + 1) * sizeof(int32_t), 256);
+}
+
+int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, int M, int epilogue,
+                     chord_bf16* C, const chord_tuning* tuning, void* workspace, size_t ws_bytes,
+                     int* dev_status, void* stream) {
+  int rc = check_tuning(tuning);
+  if (rc) return rc;
+  rc = check_gemm_shapes(N, K, epilogue);
+  if (rc) return rc;
+  if (M < 0) return fail(CHORD_ERR_INVALID_ARG, "M=%d < 0", M);
+  if (M == 0) return CHORD_OK;
+  if (!A || !packed_w || !C) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
+  if (!workspace || !aligned16(workspace)) return fail(CHORD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  const size_t need = chord_w4a16_gemm_workspace_bytes(M);
+  if (ws_bytes < need) return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "dense GEMM workspace %zu < %zu", ws_bytes, need);
+  // every row is a row of the single expert: rows per expert = M
+  const double tok_e = static_cast<double>(M);
+  chord_tuning plan{};
+  if (tuning) plan = *tuning;
+  if (!plan.path)
+    plan.path = (tok_e >= kLargeTokE && N % 128 == 0) ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
+  if (!plan.rows_per_pass) plan.rows_per_pass = rows_per_pass_for(tok_e);
+  const int bm = plan.path == CHORD_PATH_LARGE_M ? 16 : plan.rows_per_pass;
+  char* ws = static_cast<char*>(workspace);
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + kWorkBytes);
+  int32_t *counts = meta, *offsets = meta + 4, *ntpp = meta + 8;
+  int32_t* eids = reinterpret_cast<int32_t*>(ws + 2 * kWorkBytes);
+  cudaError_t e = chord::dense_setup_launch(M, bm, counts, offsets, ntpp, eids, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dense setup launch");
+  // direct rows: A is [M, K]; the tensor-core path's activation map covers
+  // exactly those M rows (reads past them return zeros)
+  return gemm_impl(A, 0, packed_w, 1, N, K, M, 1, nullptr, eids, ntpp, counts, offsets, bm,
+                   static_cast<size_t>(M), epilogue, C, &plan, tok_e, ws, kWorkBytes, dev_status, stream);
+}
+
 int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions,
                   int M, int topk, int H, chord_bf16* out, void* stream) {
   if (M < 0 || topk < 1 || H <= 0 || H % 8 != 0) return fail(CHORD_ERR_INVALID_ARG, "bad M/topk/H (H %% 8 == 0)");

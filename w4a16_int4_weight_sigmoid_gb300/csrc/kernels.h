@@ -48,6 +48,9 @@ struct GemmLaunch {
   uint16_t* C;
   int* status;
 };
+// Dense GEMM: one-expert block map (counts, offsets, ntpp, expert_ids) for M rows.
+cudaError_t dense_setup_launch(int M, int bm, int32_t* counts, int32_t* offsets, int32_t* ntpp,
+                               int32_t* expert_ids, cudaStream_t st);
 cudaError_t gemm_small_launch(const GemmLaunch& g, int rows_per_pass, cudaStream_t st);
 size_t gemm_large_smem_bytes();
 cudaError_t gemm_large_launch(const GemmLaunch& g, const uint16_t* B, size_t b_rows, cudaStream_t st);
