@@ -128,6 +128,36 @@ def test_argument_checks_reject_before_launch(L):
     assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_new_entry_points_reject_before_launch(L):
+    """chord_moe_route_align and chord_w4a16_gemm check their arguments on the host."""
+    P = ctypes.c_void_p(16)   # never dereferenced: the checks fail first
+    # route+align: topk > E_total, local experts outside E_total, bad block_m, small capacity
+    rc, msg = _rc_and_msg(L, L.chord_moe_route_align(P, P, 4, 8, 9, 0, 8, 16, 1000, P, P, P, P, P, P, P,
+                                                     None, None, 0, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "topk" in msg
+    rc, msg = _rc_and_msg(L, L.chord_moe_route_align(P, P, 4, 384, 8, 380, 8, 16, 1000, P, P, P, P, P, P, P,
+                                                     None, None, 0, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "within" in msg
+    rc, msg = _rc_and_msg(L, L.chord_moe_route_align(P, P, 4, 384, 8, 0, 48, 24, 1000, P, P, P, P, P, P, P,
+                                                     None, None, 0, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "block_m" in msg
+    rc, msg = _rc_and_msg(L, L.chord_moe_route_align(P, P, 4, 384, 8, 0, 48, 16, 10, P, P, P, P, P, P, P,
+                                                     None, None, 0, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "capacity" in msg
+    # dense GEMM: K % 64, SiLU needs N % 64, workspace too small, tcgen05 path needs N % 128
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 256, 100, 8, 0, P, None, P, 1 << 20, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 96, 128, 8, 1, P, None, P, 1 << 20, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG
+    need = L.chord_w4a16_gemm_workspace_bytes(1000)
+    assert need >= 512 + (1000 // 8) * 4
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 256, 128, 1000, 0, P, None, P, need - 1, None, None))
+    assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL
+    t = chord.chord_tuning(chord.CHORD_PATH_LARGE_M, 0, 0, 0)
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 192, 128, 1000, 0, P, ctypes.byref(t), P, need, None, None))
+    assert rc == chord.CHORD_ERR_UNSUPPORTED
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(chord, "_lib", None)
     monkeypatch.setattr(chord, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -371,6 +371,8 @@ int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, in
   if (!plan.path)
     plan.path = (tok_e >= kLargeTokE && N % 128 == 0) ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
   if (!plan.rows_per_pass) plan.rows_per_pass = rows_per_pass_for(tok_e);
+  if (plan.path == CHORD_PATH_LARGE_M && N % 128 != 0)   // checked before anything is launched
+    return fail(CHORD_ERR_UNSUPPORTED, "tcgen05 path needs N %% 128 == 0");
   const int bm = plan.path == CHORD_PATH_LARGE_M ? 16 : plan.rows_per_pass;
   char* ws = static_cast<char*>(workspace);
   int32_t* meta = reinterpret_cast<int32_t*>(ws + kWorkBytes);
