@@ -22,12 +22,15 @@
 //     into m16n8k16 A fragments (the packed order is the fragment order),
 //     take B fragments with ldmatrix, and run mma.sync with weights as the M
 //     side and tokens as N ("swap AB");
-//   * decoding is one shift and one LOP3 per register: the MMA sees q + 136
-//     (exact in BF16); per 32-wide scale group the accumulator chain is
-//     seeded with -136 * (sum of the group's activations), itself two MMAs of
-//     a constant -136 fragment, so the chain yields sum(q * x) exactly as a
-//     dot product of exact products; the group's scale is then applied in
-//     FP32 (no rounding of q * s);
+//   * decoding is one shift and one LOP3 per register, giving q + 136 as a
+//     BF16 pair (exact), then one packed BF16 add of -136 giving q exactly
+//     (the result is a small integer, so the add does not round); the MMA
+//     chain of a 32-wide scale group therefore yields sum(q * x) from exact
+//     products, and the group's scale is applied in FP32 (no rounding of
+//     q * s).  The packed add runs on the FMA pipe, which is lightly used
+//     here; an earlier form kept q + 136 and seeded each chain with
+//     -136 * sum(x) by two extra MMAs on the busier tensor pipe, and was
+//     5-12 % slower;
 //   * epilogue: SiLU(gate) * up (a gate/up slab holds gate rows g and up rows
 //     g + 8 of the same intermediate index, so both land in one thread) or a
 //     plain store, BF16, rows in sorted order.
@@ -95,10 +98,9 @@ __device__ bool header_ok(const SmallArgs& a) {
 }
 
 // One 64-wide K unit for one warp's slab and NT token tiles.  Per 32-wide
-// group: the MMA chain starts from -136 * sum(x) (two MMAs of a constant
-// -136 fragment with the group's activations) and adds (q+136)*x over the
-// group's two k16 steps, giving sum(q*x) from exact products; then
-// acc += scale * chain in FP32.  Every token tile is computed (columns of
+// group: the MMA chain starts from zero and adds q*x over the group's two
+// k16 steps, giving sum(q*x) from exact products; then acc += scale * chain
+// in FP32.  Every token tile is computed (columns of
 // unused tokens are discarded by the epilogue), so no MMA is predicated.
 template <int NT>
 __device__ __forceinline__ void unit_mma(uint32_t ub, uint32_t xu, uint32_t q_off, uint32_t s_off,
@@ -113,16 +115,18 @@ __device__ __forceinline__ void unit_mma(uint32_t ub, uint32_t xu, uint32_t q_of
     uint32_t a0[4], a1[4];
     decode_word_offset136(half ? q.z : q.x, a.nib_mask, a.nib_magic, a0);
     decode_word_offset136(half ? q.w : q.y, a.nib_mask, a.nib_magic, a1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // (q + 136) - 136: exact
+      asm("add.rn.bf16x2 %0, %0, %1;" : "+r"(a0[j]) : "r"(a.neg136));
+      asm("add.rn.bf16x2 %0, %0, %1;" : "+r"(a1[j]) : "r"(a.neg136));
+    }
     const uint32_t sw = half ? sc.y : sc.x;
     const float s_lo = bf16lo_to_f32(sw), s_hi = bf16hi_to_f32(sw);
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      const uint32_t neg136[4] = {a.neg136, a.neg136, a.neg136, a.neg136};
       const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
       float c[4];
-      mma_bf16_16816(c, neg136, bf[n][0], bf[n][1], zero4);  // -136 * sum x, k 0..15
-      mma_bf16_16816(c, neg136, bf[n][2], bf[n][3], c);      //            k 16..31
-      mma_bf16_16816(c, a0, bf[n][0], bf[n][1], c);
+      mma_bf16_16816(c, a0, bf[n][0], bf[n][1], zero4);
       mma_bf16_16816(c, a1, bf[n][2], bf[n][3], c);
       acc[n][0] = fmaf(s_lo, c[0], acc[n][0]);
       acc[n][1] = fmaf(s_lo, c[1], acc[n][1]);
