@@ -14,6 +14,8 @@ __global__ void __launch_bounds__(kThreads) align_single_kernel(AlignArgs a) {
   extern __shared__ int s[];
   __shared__ int scan_scratch[kWarps + 1];
   int loc[kPerThread], rank[kPerThread];
+  grid_dep_wait();     // topk_ids come from the router kernel
+  grid_dep_launch();
   chunk_rank(a, 0, s, loc, rank);
   int* base = sm_base(s, a.E);
   for (int e = threadIdx.x; e < a.E; e += kThreads) base[e] = 0;
@@ -25,6 +27,8 @@ __global__ void __launch_bounds__(kThreads) align_rank_kernel(AlignArgs a) {
   extern __shared__ int s[];
   const int g = blockIdx.x;
   int loc[kPerThread], rank[kPerThread];
+  grid_dep_wait();
+  grid_dep_launch();
   chunk_rank(a, g, s, loc, rank);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
@@ -41,6 +45,8 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(AlignArgs a) {
   __shared__ int scan_scratch[kWarps + 1];
   const int g = blockIdx.x, E = a.E;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_wait();
+  grid_dep_launch();
   int* tot = sm_tot(s, E);
   int* base = sm_base(s, E);
   for (int e = threadIdx.x; e < E; e += kThreads) {
@@ -60,7 +66,7 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(AlignArgs a) {
     loc[step] = -1;
     rank[step] = 0;
     if (idx < a.n) {
-      int e = a.ids[idx] - a.begin;
+      int e = ld_cg(a.ids + idx) - a.begin;
       if (e >= 0 && e < E) {
         loc[step] = e;
         rank[step] = a.ws_rank[idx];
@@ -84,7 +90,7 @@ size_t align_workspace_bytes(long long n, int E_local) {
 
 cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_local, int bm,
                          int32_t* sorted, int32_t* expert_ids, int32_t* ntpp, int32_t* counts,
-                         int32_t* offsets, int32_t* positions, void* ws, cudaStream_t st) {
+                         int32_t* offsets, int32_t* positions, void* ws, cudaStream_t st, bool pdl) {
   AlignArgs a;
   a.ids = ids;
   a.n = M * topk;
@@ -107,12 +113,8 @@ cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_l
   if (err == cudaSuccess) err = ensure_smem_limit<align_rank_kernel>(max_smem);
   if (err == cudaSuccess) err = ensure_smem_limit<align_scatter_kernel>(max_smem);
   if (err != cudaSuccess) return err;
-  if (a.G == 1) {
-    align_single_kernel<<<1, kThreads, smem, st>>>(a);
-    return cudaGetLastError();
-  }
-  align_rank_kernel<<<a.G, kThreads, smem, st>>>(a);
-  err = cudaGetLastError();
+  if (a.G == 1) return launch_kernel(align_single_kernel, dim3(1), dim3(kThreads), smem, st, pdl, a);
+  err = launch_kernel(align_rank_kernel, dim3(a.G), dim3(kThreads), smem, st, pdl, a);
   if (err != cudaSuccess) return err;
   align_scatter_kernel<<<a.G, kThreads, smem, st>>>(a);
   return cudaGetLastError();

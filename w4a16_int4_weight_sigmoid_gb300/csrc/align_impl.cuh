@@ -57,7 +57,7 @@ __device__ void chunk_rank(const AlignArgs& a, int g, int* s, int (&loc)[kPerThr
     const int idx = elem_index(g, warp, step, lane);
     int e = -1;
     if (idx < a.n) {
-      e = a.ids[idx] - a.begin;
+      e = ld_cg(a.ids + idx) - a.begin;   // ordered L2 load: ids may come from the preceding kernel
       if (e < 0 || e >= E) e = -1;
     }
     const uint32_t peers = __match_any_sync(0xffffffffu, e);

@@ -159,11 +159,16 @@ size_t chord_moe_align_workspace_bytes(int M, int topk, int E_local) {
   return chord::align_workspace_bytes(static_cast<long long>(M) * topk, E_local);
 }
 
-int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, int E_local,
-                    int block_m, size_t capacity, int32_t* sorted_token_ids, int32_t* expert_ids,
-                    int32_t* num_tokens_post_padded, int32_t* expert_counts,
-                    int32_t* expert_offsets, int32_t* sorted_positions, void* workspace,
-                    size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// chord_moe_align with a choice of programmatic launch (pdl: the align may
+// start before the router kernel ends and waits for it).
+int align_impl(const int32_t* topk_ids, int M, int topk, int expert_begin, int E_local, int block_m,
+               size_t capacity, int32_t* sorted_token_ids, int32_t* expert_ids,
+               int32_t* num_tokens_post_padded, int32_t* expert_counts, int32_t* expert_offsets,
+               int32_t* sorted_positions, void* workspace, size_t ws_bytes, void* stream, bool pdl) {
   if (M < 0 || topk < 1 || topk > 32) return fail(CHORD_ERR_INVALID_ARG, "bad M=%d or topk=%d", M, topk);
   if (E_local < 1 || E_local > 1024) return fail(CHORD_ERR_INVALID_ARG, "E_local=%d not in [1, 1024]", E_local);
   if (expert_begin < 0) return fail(CHORD_ERR_INVALID_ARG, "expert_begin=%d < 0", expert_begin);
@@ -180,8 +185,30 @@ int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, 
   cudaError_t e = chord::align_launch(topk_ids, M, topk, expert_begin, E_local, block_m,
                                       sorted_token_ids, expert_ids, num_tokens_post_padded,
                                       expert_counts, expert_offsets, sorted_positions, workspace,
-                                      static_cast<cudaStream_t>(stream));
+                                      static_cast<cudaStream_t>(stream), pdl);
   return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "align launch");
+}
+
+// chord_moe_route_align with a programmatic launch of the align kernel
+// after the router kernel (pdl) when the two are separate launches.
+int route_align_impl(const float* logits, const float* bias, int M, int E_total, int topk,
+                     int expert_begin, int E_local, int block_m, size_t capacity, float* topk_weights,
+                     int32_t* topk_ids, int32_t* sorted_token_ids, int32_t* expert_ids,
+                     int32_t* num_tokens_post_padded, int32_t* expert_counts, int32_t* expert_offsets,
+                     int32_t* sorted_positions, void* workspace, size_t ws_bytes, void* stream, bool pdl);
+
+}  // namespace
+
+extern "C" {
+
+int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, int E_local,
+                    int block_m, size_t capacity, int32_t* sorted_token_ids, int32_t* expert_ids,
+                    int32_t* num_tokens_post_padded, int32_t* expert_counts,
+                    int32_t* expert_offsets, int32_t* sorted_positions, void* workspace,
+                    size_t ws_bytes, void* stream) {
+  return align_impl(topk_ids, M, topk, expert_begin, E_local, block_m, capacity, sorted_token_ids,
+                    expert_ids, num_tokens_post_padded, expert_counts, expert_offsets, sorted_positions,
+                    workspace, ws_bytes, stream, false);
 }
 
 int chord_moe_route_align(const float* logits, const float* bias, int M, int E_total, int topk,
@@ -190,6 +217,21 @@ int chord_moe_route_align(const float* logits, const float* bias, int M, int E_t
                           int32_t* expert_ids, int32_t* num_tokens_post_padded, int32_t* expert_counts,
                           int32_t* expert_offsets, int32_t* sorted_positions, void* workspace,
                           size_t ws_bytes, void* stream) {
+  return route_align_impl(logits, bias, M, E_total, topk, expert_begin, E_local, block_m, capacity,
+                          topk_weights, topk_ids, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                          expert_counts, expert_offsets, sorted_positions, workspace, ws_bytes, stream,
+                          false);
+}
+
+}  // extern "C"
+
+namespace {
+
+int route_align_impl(const float* logits, const float* bias, int M, int E_total, int topk,
+                     int expert_begin, int E_local, int block_m, size_t capacity, float* topk_weights,
+                     int32_t* topk_ids, int32_t* sorted_token_ids, int32_t* expert_ids,
+                     int32_t* num_tokens_post_padded, int32_t* expert_counts, int32_t* expert_offsets,
+                     int32_t* sorted_positions, void* workspace, size_t ws_bytes, void* stream, bool pdl) {
   if (M < 0) return fail(CHORD_ERR_INVALID_ARG, "M=%d < 0", M);
   if (E_total < 1 || E_total > 1024) return fail(CHORD_ERR_INVALID_ARG, "E_total=%d not in [1, 1024]", E_total);
   if (topk < 1 || topk > E_total || topk > 32)
@@ -209,9 +251,9 @@ int chord_moe_route_align(const float* logits, const float* bias, int M, int E_t
     // more than one chunk: the two separate launches
     int rc = chord_moe_route(logits, bias, M, E_total, topk, topk_weights, topk_ids, stream);
     if (rc) return rc;
-    return chord_moe_align(topk_ids, M, topk, expert_begin, E_local, block_m, capacity, sorted_token_ids,
-                           expert_ids, num_tokens_post_padded, expert_counts, expert_offsets,
-                           sorted_positions, workspace, ws_bytes, stream);
+    return align_impl(topk_ids, M, topk, expert_begin, E_local, block_m, capacity, sorted_token_ids,
+                      expert_ids, num_tokens_post_padded, expert_counts, expert_offsets, sorted_positions,
+                      workspace, ws_bytes, stream, pdl);
   }
   cudaError_t e = chord::route_align_launch(logits, bias, M, E_total, topk, expert_begin, E_local, block_m,
                                             topk_weights, topk_ids, sorted_token_ids, expert_ids,
@@ -219,6 +261,10 @@ int chord_moe_route_align(const float* logits, const float* bias, int M, int E_t
                                             sorted_positions, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "route+align launch");
 }
+
+}  // namespace
+
+extern "C" {
 
 int chord_moe_align_noalloc(const int32_t* topk_ids, int M, int topk, int expert_begin, int E_local,
                             int block_m, size_t capacity, int32_t* sorted_token_ids,
@@ -270,7 +316,7 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
                      const int32_t* expert_ids, const int32_t* ntpp, const int32_t* expert_counts,
                      const int32_t* expert_offsets, int block_m, size_t capacity, int epilogue,
                      chord_bf16* C, const chord_tuning* tuning, double tok_e, void* workspace,
-                     size_t ws_bytes, int* dev_status, void* stream) {
+                     size_t ws_bytes, int* dev_status, void* stream, int pdl = 0) {
   int rc = check_tuning(tuning);
   if (rc) return rc;
   rc = check_gemm_shapes(N, K, epilogue);
@@ -308,6 +354,9 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
   g.epilogue = epilogue;
   g.C = C;
   g.status = dev_status;
+  g.pdl = pdl;
+  const size_t max_blocks = (capacity + block_m - 1) / block_m;
+  g.max_blocks = max_blocks > 0x7fffffff ? 0x7fffffff : static_cast<int>(max_blocks);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (path == CHORD_PATH_LARGE_M) {
@@ -386,14 +435,29 @@ int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, in
                    static_cast<size_t>(M), epilogue, C, &plan, tok_e, ws, kWorkBytes, dev_status, stream);
 }
 
-int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions,
-                  int M, int topk, int H, chord_bf16* out, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// chord_moe_sum with a choice of programmatic launch (pdl: may start before
+// the down GEMM ends and waits for it).
+int moe_sum_impl(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions, int M,
+                 int topk, int H, chord_bf16* out, void* stream, bool pdl) {
   if (M < 0 || topk < 1 || H <= 0 || H % 8 != 0) return fail(CHORD_ERR_INVALID_ARG, "bad M/topk/H (H %% 8 == 0)");
   if (M > 0 && (!y || !topk_weights || !sorted_positions || !out)) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(y) || !aligned16(out)) return fail(CHORD_ERR_INVALID_ARG, "y and out must be 16-byte aligned");
   cudaError_t e = chord::moe_sum_launch(y, topk_weights, sorted_positions, M, topk, H, out,
-                                        static_cast<cudaStream_t>(stream));
+                                        static_cast<cudaStream_t>(stream), pdl);
   return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "moe_sum launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions,
+                  int M, int topk, int H, chord_bf16* out, void* stream) {
+  return moe_sum_impl(y, topk_weights, sorted_positions, M, topk, H, out, stream, false);
 }
 
 int chord_moe_layer_plan(int M, int E_total, int topk, chord_tuning* plan) {
@@ -456,20 +520,26 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
 
   cudaError_t ce = cudaMemsetAsync(ws + w.work, 0, 2 * kWorkBytes, st);
   if (ce != cudaSuccess) return cuda_fail(ce, "work counter reset");
+  // Register-MMA path: every kernel after the router is a programmatic
+  // launch, so its launch and prologue overlap the end of the kernel before
+  // it, and the down GEMM streams its first weight stages while the gate/up
+  // GEMM finishes.  The tcgen05 path launches in plain stream order.
+  const bool pdl = plan.path != CHORD_PATH_LARGE_M;
   // one launch when the assignments fit one align chunk, else two
-  rc = chord_moe_route_align(logits, bias, M, E_total, topk, expert_begin, E_local, w.bm, w.cap, tw, ids,
-                             sorted, eids, ntpp, counts, offsets, pos, aws,
-                             chord_moe_align_workspace_bytes(M, topk, E_local), stream);
+  rc = route_align_impl(logits, bias, M, E_total, topk, expert_begin, E_local, w.bm, w.cap, tw, ids, sorted,
+                        eids, ntpp, counts, offsets, pos, aws, chord_moe_align_workspace_bytes(M, topk, E_local),
+                        stream, pdl);
   if (rc) return rc;
   const double tok_e = static_cast<double>(M) * topk / E_total;
   rc = gemm_impl(x, 1, w13_packed, E_local, 2 * I, H, M, topk, sorted, eids, ntpp, counts, offsets,
                  w.bm, w.cap, CHORD_EPI_SILU_MUL, h, &plan, tok_e, ws + w.work + kWorkBytes,
-                 kWorkBytes + w.cap * static_cast<size_t>(H) * 2, dev_status, stream);
+                 kWorkBytes + w.cap * static_cast<size_t>(H) * 2, dev_status, stream, pdl ? 1 : 0);
   if (rc) return rc;
   rc = gemm_impl(h, 0, w2_packed, E_local, H, I, M, topk, sorted, eids, ntpp, counts, offsets, w.bm,
-                 w.cap, CHORD_EPI_STORE, y, &plan, tok_e, ws + w.work, kWorkBytes, dev_status, stream);
+                 w.cap, CHORD_EPI_STORE, y, &plan, tok_e, ws + w.work, kWorkBytes, dev_status, stream,
+                 pdl ? 2 : 0);
   if (rc) return rc;
-  return chord_moe_sum(y, tw, pos, M, topk, H, out, stream);
+  return moe_sum_impl(y, tw, pos, M, topk, H, out, stream, pdl);
 }
 
 }  // extern "C"

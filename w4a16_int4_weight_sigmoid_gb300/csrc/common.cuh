@@ -37,6 +37,66 @@ struct PackHeader {
 };
 static_assert(sizeof(PackHeader) <= kPackHeaderBytes, "header too large");
 
+// Programmatic dependent launch.  A kernel launched with
+// launch_kernel(..., pdl = true) may start while the previous kernel in the
+// stream is still running; grid_dep_wait() returns once that kernel has
+// completed and its writes are visible (at once for an ordinary launch), so
+// it must come before any read of what the previous kernels wrote.  Those
+// reads must not use __ldg / ld.global.nc: the compiler treats such a load
+// as invariant and may move it above the wait (measured: stale block counts
+// in the GEMM after the wait); they use ld_ca / ld_cg / ld_cg_v4 below,
+// which stay in program order.
+// grid_dep_launch() lets the next programmatic launch be scheduled once
+// every CTA of this grid has issued it or exited; the kernels here issue it
+// only after their own grid_dep_wait(), so a kernel two launches later
+// always finds the outputs of the one before its predecessor complete.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Global loads cached in L2 only (no L1 or texture-cache copy), kept in
+// program order relative to the other inline-assembly statements.
+__device__ __forceinline__ int ld_cg(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+// Same, cached in L1 as well: for small data read many times after the wait
+// (the wait makes the preceding grid's writes visible to ordinary loads).
+__device__ __forceinline__ int ld_ca(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.ca.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_cg(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Launch a kernel, with programmatic stream serialization when pdl is set.
+template <typename... P, typename... A>
+inline cudaError_t launch_kernel(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 bool pdl, A&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+}
+
 __device__ __forceinline__ void set_status(int* st, int code) {
   if (st) atomicCAS(st, 0, code);
 }

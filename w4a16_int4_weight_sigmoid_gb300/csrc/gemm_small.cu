@@ -69,6 +69,7 @@ struct SmallArgs {
   uint16_t* C;
   int* status;
   int N, K, topk, ldc, n_tiles, E_local;
+  int pdl, max_blocks;   // programmatic-launch mode (GemmLaunch::pdl); capacity / block_m
   int64_t tile_bytes;
   uint32_t need_flags;
   // decode constants, passed at run time so they stay in registers
@@ -173,21 +174,110 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     // counter; each is pushed to the consumers through a small ring and its
     // stages are streamed into the shared ring.  The last CTA to run out of
     // items zeroes the counters for the next launch.
-    const int nblocks = __ldg(a.ntpp) / a.block_m;
-    const long long total = static_cast<long long>(a.n_tiles) * nblocks;
-    int it = 0, q = 0;
-    bool ok = true;
-    while (ok) {
-      int i = 0;
-      if (lane == 0) i = atomicAdd(a.work, 1);
-      i = __shfl_sync(0xffffffffu, i, 0);
+    //
+    // Programmatic launch: mode 1 waits for the previous kernel before
+    // anything else.  Mode 2 reads the expert map and issues the weight
+    // copies of the first stages before the wait (weights are never written
+    // by the kernels of a layer, and the expert map is complete at launch);
+    // the activation rows, the previous kernel's output, follow the wait.
+    // The consumers read global memory only through these copies.
+    //
+    // Item i -> (tile, expert, first sorted row, rows); rows = -1 past the
+    // end, 0 for a block whose expert id is out of range (recorded).
+    // Loads of the expert map: through the read-only cache in an ordinary
+    // launch; in a programmatic one, ordered loads (see grid_dep_wait), from
+    // L2 only before the wait.
+    auto ld_map = [&](const int32_t* p, int how) {
+      return how == 0 ? __ldg(p) : how == 1 ? ld_ca(p) : ld_cg(p);
+    };
+    const int how = a.pdl ? 1 : 0;   // after the wait
+    auto decode_item = [&](int i, long long total, int nblocks, int how) {
       int4 item = make_int4(0, 0, 0, -1);
       if (i < total) {
         const int nt = i / nblocks, b = i - nt * nblocks;
-        const int e = __ldg(a.expert_ids + b);
-        const int row0 = b * a.block_m;
-        const int rows = min(a.block_m, __ldg(a.offsets + e) + __ldg(a.counts + e) - row0);
-        item = make_int4(nt, e, row0, rows);
+        const int e = ld_map(a.expert_ids + b, how);
+        item = make_int4(nt, 0, 0, 0);
+        if (e >= 0 && e < a.E_local) {
+          const int row0 = b * a.block_m;
+          const int end = ld_map(a.offsets + e, how) + ld_map(a.counts + e, how);
+          item = make_int4(nt, e, row0, max(min(a.block_m, end - row0), 0));
+        } else {
+          set_status(a.status, CHORD_ERR_ROUTING_INVALID);
+        }
+      }
+      return item;
+    };
+    auto weight_tile = [&](const int4& item) {
+      return a.packed + kPackHeaderBytes +
+             (static_cast<size_t>(item.y) * a.n_tiles + item.x) * static_cast<size_t>(a.tile_bytes);
+    };
+    // weights of stage ks into ring slot s, the slot expecting `rows` rows too
+    auto issue_weights = [&](const uint8_t* wtile, int rows, int ks, int s) {
+      const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full_bar[s], units * kUnitBytes + rows * units * kUnitK * 2);
+        bulk_g2s(smem + s * Cfg::kStageBytes, wtile + static_cast<size_t>(ks) * kUnitsPerStage * kUnitBytes,
+                 units * kUnitBytes, &full_bar[s]);
+      }
+      __syncwarp();
+    };
+    // activation rows of stage ks of one pass into ring slot s
+    auto issue_rows = [&](const int4& item, int pass, int rows, int ks, int s) {
+      const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
+      const uint32_t xbytes = units * kUnitK * 2;
+      uint8_t* st = smem + s * Cfg::kStageBytes;
+      for (int j = lane; j < rows; j += 32) {
+        const int r = item.z + pass * Cfg::kRowsPerPass + j;
+        const int row = GATHER ? ld_map(a.sorted + r, how) / a.topk : r;
+        const uint16_t* src = a.A + static_cast<size_t>(row) * a.K + ks * kUnitsPerStage * kUnitK;
+        bulk_g2s(st + Cfg::kWBytes + j * kXPitch, src, xbytes, &full_bar[s]);
+      }
+    };
+    int nblocks = 0;
+    int4 first = make_int4(0, 0, 0, -1);
+    int pre = 0;   // stages of the first item's first pass already issued
+    if (a.pdl == 2) {
+      // The expert map is read from L2 here, never from a copy an SM cached
+      // before it was written.
+      nblocks = ld_cg(a.ntpp) / a.block_m;
+    } else {
+      if (a.pdl) {
+        grid_dep_wait();
+        grid_dep_launch();
+      }
+      nblocks = ld_map(a.ntpp, how) / a.block_m;
+    }
+    if (nblocks > a.max_blocks || nblocks < 0) {
+      set_status(a.status, CHORD_ERR_INVALID_ARG);
+      nblocks = nblocks < 0 ? 0 : a.max_blocks;
+    }
+    const long long total = static_cast<long long>(a.n_tiles) * nblocks;
+    if (a.pdl == 2) {
+      int i = 0;
+      if (lane == 0) i = atomicAdd(a.work, 1);
+      i = __shfl_sync(0xffffffffu, i, 0);
+      first = decode_item(i, total, nblocks, 2);
+      const int rows0 = min(Cfg::kRowsPerPass, first.w);
+      if (rows0 > 0) {
+        pre = min(STAGES, k_stages);
+        for (int ks = 0; ks < pre; ++ks) issue_weights(weight_tile(first), rows0, ks, ks);
+      }
+      grid_dep_wait();
+      grid_dep_launch();
+      for (int ks = 0; ks < pre; ++ks) issue_rows(first, 0, rows0, ks, ks);
+    }
+    int it = 0, q = 0;
+    bool ok = true, use_first = a.pdl == 2;
+    while (ok) {
+      int4 item;
+      if (use_first) {   // fetched before the wait
+        item = first;
+        use_first = false;
+      } else {
+        int i = 0;
+        if (lane == 0) i = atomicAdd(a.work, 1);
+        i = __shfl_sync(0xffffffffu, i, 0);
+        item = decode_item(i, total, nblocks, how);
       }
       const int slot = q % kItemSlots;
       if (q >= kItemSlots)
@@ -200,32 +290,21 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       }
       ++q;
       if (item.w < 0) break;
-      const uint8_t* wtile = a.packed + kPackHeaderBytes +
-                             (static_cast<size_t>(item.y) * a.n_tiles + item.x) *
-                                 static_cast<size_t>(a.tile_bytes);
+      const uint8_t* wtile = weight_tile(item);
       const int passes = (item.w + Cfg::kRowsPerPass - 1) / Cfg::kRowsPerPass;
       for (int pass = 0; pass < passes && ok; ++pass) {
         const int rows = min(Cfg::kRowsPerPass, item.w - pass * Cfg::kRowsPerPass);
         for (int ks = 0; ks < k_stages; ++ks, ++it) {
+          if (pre > 0) {   // issued before the wait (first pass of the first item: it == ks)
+            --pre;
+            continue;
+          }
           const int s = it % STAGES;
           if (it >= STAGES) ok = mbar_wait_backoff(&empty_bar[s], ((it / STAGES) - 1) & 1, a.status);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
-          const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
-          const uint32_t xbytes = units * kUnitK * 2;
-          uint8_t* st = smem + s * Cfg::kStageBytes;
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&full_bar[s], units * kUnitBytes + rows * xbytes);
-            bulk_g2s(st, wtile + static_cast<size_t>(ks) * kUnitsPerStage * kUnitBytes,
-                     units * kUnitBytes, &full_bar[s]);
-          }
-          __syncwarp();
-          for (int j = lane; j < rows; j += 32) {
-            const int r = item.z + pass * Cfg::kRowsPerPass + j;
-            const int row = GATHER ? __ldg(a.sorted + r) / a.topk : r;
-            const uint16_t* src = a.A + static_cast<size_t>(row) * a.K + ks * kUnitsPerStage * kUnitK;
-            bulk_g2s(st + Cfg::kWBytes + j * kXPitch, src, xbytes, &full_bar[s]);
-          }
+          issue_weights(wtile, rows, ks, s);
+          issue_rows(item, pass, rows, ks, s);
         }
       }
     }
@@ -326,8 +405,7 @@ cudaError_t launch_small(const SmallArgs& a, cudaStream_t st) {
     sms[dev] = m;
     per_sm[dev] = n > 0 ? n : 1;
   }
-  gemm_small_kernel<NT, STAGES, GATHER, EPI><<<per_sm[dev] * sms[dev], kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(per_sm[dev] * sms[dev]), dim3(kThreads), smem, st, a.pdl != 0, a);
 }
 
 template <int NT, int STAGES>
@@ -359,6 +437,8 @@ cudaError_t gemm_small_launch(const GemmLaunch& g, int rows_per_pass, cudaStream
   a.K = g.K;
   a.topk = g.topk;
   a.E_local = g.E_local;
+  a.pdl = g.pdl;
+  a.max_blocks = g.max_blocks;
   const PackHeader h = make_pack_header(g.E_local, g.N, g.K, g.epilogue == CHORD_EPI_SILU_MUL);
   a.n_tiles = h.n_tiles;
   a.tile_bytes = h.tile_bytes;

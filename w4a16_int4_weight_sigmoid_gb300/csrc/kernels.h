@@ -22,7 +22,8 @@ cudaError_t route_align_launch(const float* logits, const float* bias, int M, in
                                int32_t* positions, cudaStream_t st);
 cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_local, int bm,
                          int32_t* sorted, int32_t* expert_ids, int32_t* ntpp, int32_t* counts,
-                         int32_t* offsets, int32_t* positions, void* ws, cudaStream_t st);
+                         int32_t* offsets, int32_t* positions, void* ws, cudaStream_t st,
+                         bool pdl = false);
 
 cudaError_t align_noalloc_scratch(void** ptr);
 size_t align_noalloc_scratch_bytes();
@@ -47,6 +48,13 @@ struct GemmLaunch {
   int epilogue;
   uint16_t* C;
   int* status;
+  // Programmatic launch (small-M path only): 0 ordinary; 1 the kernel may
+  // start before the previous kernel ends and waits for it before reading
+  // anything; 2 as 1, and the expert map (ntpp, expert_ids, counts, offsets)
+  // is already complete at launch, so the first weight stages are fetched
+  // before the wait (the previous kernel is a GEMM launched with mode 1).
+  int pdl = 0;
+  int max_blocks = 0;   // BLOCK_M blocks the aligned buffers hold (capacity / block_m)
 };
 // Dense GEMM: one-expert block map (counts, offsets, ntpp, expert_ids) for M rows.
 cudaError_t dense_setup_launch(int M, int bm, int32_t* counts, int32_t* offsets, int32_t* ntpp,
@@ -58,6 +66,6 @@ cudaError_t gather_rows_launch(const uint16_t* x, const int32_t* sorted, const i
                                int sentinel, int K, size_t capacity, uint16_t* out, cudaStream_t st);
 
 cudaError_t moe_sum_launch(const uint16_t* y, const float* w, const int32_t* pos, int M, int topk,
-                           int H, uint16_t* out, cudaStream_t st);
+                           int H, uint16_t* out, cudaStream_t st, bool pdl = false);
 
 }  // namespace chord

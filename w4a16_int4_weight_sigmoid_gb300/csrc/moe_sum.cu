@@ -10,11 +10,15 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kColsPerCta = kThreads * 8;
 
-__global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* __restrict__ y,
-                                                           const float* __restrict__ w,
-                                                           const int32_t* __restrict__ pos,
-                                                           int topk, int H,
+// kOrdered: a programmatic launch; y, w and pos come from kernels that may
+// still be running when this grid starts, so they are read after the wait
+// with ordered L2 loads (see grid_dep_wait), not through the read-only cache.
+template <bool kOrdered>
+__global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* y, const float* w,
+                                                           const int32_t* pos, int topk, int H,
                                                            uint16_t* __restrict__ out) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int t = blockIdx.x;
   const int c = blockIdx.y * kColsPerCta + threadIdx.x * 8;
   if (c >= H) return;
@@ -30,14 +34,17 @@ __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* __res
     for (int j = 0; j < 8; ++j) {
       const bool in = j0 + j < topk;
       const size_t o = static_cast<size_t>(t) * topk + (in ? j0 + j : 0);
-      p[j] = in ? __ldg(pos + o) : -1;
-      wj[j] = in ? __ldg(w + o) : 0.f;
+      p[j] = in ? (kOrdered ? ld_cg(pos + o) : __ldg(pos + o)) : -1;
+      wj[j] = in ? (kOrdered ? ld_cg(w + o) : __ldg(w + o)) : 0.f;
     }
     uint4 v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       v[j] = make_uint4(0, 0, 0, 0);
-      if (p[j] >= 0) v[j] = __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(p[j]) * H + c));
+      if (p[j] >= 0) {
+        const uint16_t* src = y + static_cast<size_t>(p[j]) * H + c;
+        v[j] = kOrdered ? ld_cg_v4(src) : __ldg(reinterpret_cast<const uint4*>(src));
+      }
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -60,11 +67,11 @@ __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* __res
 }  // namespace
 
 cudaError_t moe_sum_launch(const uint16_t* y, const float* w, const int32_t* pos, int M, int topk,
-                           int H, uint16_t* out, cudaStream_t st) {
+                           int H, uint16_t* out, cudaStream_t st, bool pdl) {
   if (M == 0) return cudaSuccess;
   dim3 grid(M, (H + kColsPerCta - 1) / kColsPerCta);
-  moe_sum_kernel<<<grid, kThreads, 0, st>>>(y, w, pos, topk, H, out);
-  return cudaGetLastError();
+  if (pdl) return launch_kernel(moe_sum_kernel<true>, grid, dim3(kThreads), 0, st, true, y, w, pos, topk, H, out);
+  return launch_kernel(moe_sum_kernel<false>, grid, dim3(kThreads), 0, st, false, y, w, pos, topk, H, out);
 }
 
 }  // namespace chord

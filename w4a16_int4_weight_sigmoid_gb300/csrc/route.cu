@@ -14,6 +14,8 @@ __global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ lo
                                                     const float* __restrict__ bias, int M, int E,
                                                     int topk, float* __restrict__ w_out,
                                                     int32_t* __restrict__ id_out) {
+  grid_dep_wait();     // logits may come from the previous kernel
+  grid_dep_launch();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= M) return;
   route_token<EPL>(logits, bias, t, E, topk, w_out, id_out);

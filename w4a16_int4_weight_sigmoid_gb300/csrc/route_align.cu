@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(kThreads) route_align_kernel(RouteIn r, AlignA
   extern __shared__ int s[];
   __shared__ int scan_scratch[kWarps + 1];
   const int warp = threadIdx.x >> 5;
+  grid_dep_wait();
+  grid_dep_launch();
   for (int t = warp; t < r.M; t += kWarps) route_token<EPL>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
   __syncthreads();   // this CTA's topk_ids stores are visible to all its threads
   int loc[kPerThread], rank[kPerThread];
