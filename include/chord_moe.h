@@ -281,6 +281,12 @@ int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t*
  * The expert-parallel shard is implied by E_local < E_total ([Chord]
  * "런타임 고려사항": the profile is inferred from the shapes, no shard
  * argument).  Weights are normalised over all topk experts, local or not.
+ * Launch order: the first kernel is an ordinary launch, so the call starts
+ * after all earlier work in the stream.  On the register-MMA path every
+ * later kernel of the call is a programmatic dependent launch: it may start
+ * before the previous kernel of the call ends and waits for it before
+ * reading its outputs (captured into a CUDA graph, these become programmatic
+ * edges).  Work enqueued after the call starts after its last kernel ends.
  */
 size_t chord_moe_layer_workspace_bytes(int M, int H, int I, int E_local, int topk);
 /* Host-only: the tuning chord_moe_layer uses for these shapes (tokens-per-

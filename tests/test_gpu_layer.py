@@ -48,6 +48,34 @@ SMALL = [
 ]
 
 
+def test_layer_fresh_workspace_every_call():
+    """The register-MMA path chains its kernels with programmatic launches:
+    each kernel must read the previous kernel's outputs only after waiting
+    for it.  A fresh workspace per call, filled with a pattern that cannot
+    be a valid block map (0x7F bytes) or with zeros, exposes any read that
+    comes too early, as a device status or as a wrong output."""
+    shape = small("tp_zipf_fresh_ws", 48, 256, 192, 32, 32, 0, 6, 22, zipf=1.1)
+    d = wl.layer_inputs(shape)
+    ref, _, _ = oracle.moe_layer(d["x"], d["logits"], d["bias"], d["w13_q"], d["w13_s"],
+                                 d["w2_q"], d["w2_s"], shape.topk, shape.expert_begin)
+    layer = W4A16MoELayer(d["w13_q"], d["w13_s"], d["w2_q"], d["w2_s"], shape.E_total,
+                          shape.expert_begin, shape.topk)
+    x, lg, b = to_device(d["x"]), to_device(d["logits"]), to_device(d["bias"])
+    n = layer.workspace(shape.M).numel()
+    first = None
+    for i in range(40):
+        layer._ws = torch.full((n,), 0x7F if i % 2 else 0, dtype=torch.uint8, device="cuda")
+        out = layer.forward(x, lg, b)
+        torch.cuda.synchronize()
+        assert layer.dev_status.item() == 0, f"call {i}: device status {layer.dev_status.item()}"
+        got = bf16_to_np(out)
+        if first is None:
+            assert_close_to_oracle(got, ref, shape.name)
+            first = got
+        else:
+            assert np.array_equal(got, first), f"call {i} differs"
+
+
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
 def test_layer_small_full_parity(shape):
     d = wl.layer_inputs(shape)
