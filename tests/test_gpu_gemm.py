@@ -135,11 +135,14 @@ def test_gemm_direct_rows_and_header_check(path):
     assert status.item() == chord.CHORD_ERR_PREPACK_MISMATCH
 
 
-def test_moe_sum_against_oracle():
-    M, k, H, E = 37, 4, 1024, 12
+# (M, topk, H, E_total, local experts): one CTA per (token, column block),
+# and the streaming form taken from 4096 items on (1100 tokens x 4 column
+# blocks, the last one ragged: H = 3976)
+@pytest.mark.parametrize("M,k,H,E,local", [(37, 4, 1024, 12, (2, 7)), (1100, 6, 3976, 40, (3, 25))])
+def test_moe_sum_against_oracle(M, k, H, E, local):
     logits, bias = wl.router_inputs(M, E, 12)
     w, ids, _ = oracle.route(logits, bias, k)
-    al = oracle.moe_align(ids, 2, 7, 16)          # some assignments dropped
+    al = oracle.moe_align(ids, local[0], local[1], 16)   # some assignments dropped
     cap = max(al["num_tokens_post_padded"], 1)
     y = wl.activations(cap, H, 13)
     out = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
