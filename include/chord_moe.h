@@ -257,6 +257,43 @@ int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, in
                      chord_bf16* C, const chord_tuning* tuning, void* workspace, size_t ws_bytes,
                      int* dev_status, void* stream);
 
+/* ------------------------------------------------------- grouped layouts
+ * The grouped kernels' activation layouts ([Chord] "그룹 SM90 커널 기법":
+ * contiguous prefill pads each expert to a 128-row boundary; masked decode
+ * reserves a fixed row budget per expert and picks BLOCK_M from the expected
+ * token count).  The rows are already grouped by expert: no routing, no
+ * gather.  For each expert e and each of its group_rows[e] rows r:
+ *   C[r, :] = A[r, :] (q_e s_e)^T          (epilogue CHORD_EPI_STORE), or
+ *   C[r, :] = SiLU(gate) * up              (CHORD_EPI_SILU_MUL, N = 2I)
+ * with packed_w the prepacked [E, N, K] blob (gate_up = 1 for SiLU*mul).
+ *   contiguous: A BF16 [a_rows, K]; expert e's rows start at
+ *     sum_{e' < e} ceil(group_rows[e'] / 128) * 128 and run for
+ *     group_rows[e]; the padded total must be <= a_rows.
+ *   masked: A BF16 [E, max_m, K] (max_m a multiple of 16); expert e's rows
+ *     are its first group_rows[e] <= max_m rows.
+ *   group_rows   device INT32 [E], 1 <= E <= 1024
+ *   expected_m   rows per expert the plan assumes (<= 0: a_rows / E for
+ *                contiguous, max_m for masked): picks the register-MMA or
+ *                tcgen05 path and BLOCK_M, as chord_w4a16_moe_gemm does
+ *   C            BF16, the same row layout as A, N (STORE) or N/2 columns;
+ *                rows past an expert's group_rows are not written
+ *   workspace    chord_w4a16_grouped_workspace_bytes(E, rows of A) bytes,
+ *                16-byte aligned, its first 256 bytes zeroed once when
+ *                allocated (kept zero by every call)
+ * Host-side errors return CHORD_ERR_* and launch nothing; a count outside
+ * [0, max_m] (masked) or a padded total above the rows of A (contiguous) is
+ * recorded in *dev_status as CHORD_ERR_INVALID_ARG and nothing is computed.
+ */
+size_t chord_w4a16_grouped_workspace_bytes(int E, size_t rows);
+int chord_w4a16_grouped_gemm_contiguous(const chord_bf16* A, size_t a_rows, const int32_t* group_rows, int E,
+                                        int expected_m, const void* packed_w, int N, int K, int epilogue,
+                                        chord_bf16* C, const chord_tuning* tuning, void* workspace,
+                                        size_t ws_bytes, int* dev_status, void* stream);
+int chord_w4a16_grouped_gemm_masked(const chord_bf16* A, const int32_t* group_rows, int E, int max_m,
+                                    int expected_m, const void* packed_w, int N, int K, int epilogue,
+                                    chord_bf16* C, const chord_tuning* tuning, void* workspace, size_t ws_bytes,
+                                    int* dev_status, void* stream);
+
 /* --------------------------------------------------------- top-k weighted sum
  * moe_fused_mul_sum ([HumPR] "왜 이게 좋은가" 3: weight multiply and sum):
  *   out[t, :] = sum over j = 0..topk-1 with sorted_positions[t*topk+j] >= 0 of

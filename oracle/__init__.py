@@ -36,9 +36,11 @@ from .align import align_capacity, moe_align
 from .quant import bf16_to_f64, unpack_int4, dequant, dequant_expert
 from .layer import (silu, expert_rows_gemm, silu_mul, moe_sum, moe_layer,
                     moe_layer_tokens)
+from .grouped import group_starts, grouped_gemm
 
 __all__ = [
     "sigmoid_binary32", "exp_binary32", "route", "align_capacity", "moe_align",
     "bf16_to_f64", "unpack_int4", "dequant", "dequant_expert", "silu",
     "expert_rows_gemm", "silu_mul", "moe_sum", "moe_layer", "moe_layer_tokens",
+    "group_starts", "grouped_gemm",
 ]

@@ -158,6 +158,42 @@ def test_new_entry_points_reject_before_launch(L):
     assert rc == chord.CHORD_ERR_UNSUPPORTED
 
 
+def test_grouped_entry_points_reject_before_launch(L):
+    """The grouped-layout GEMMs check their arguments on the host; every case
+    below fails a check, so nothing is launched with these placeholder pointers."""
+    P = ctypes.c_void_p(16)
+    assert L.chord_w4a16_grouped_workspace_bytes(0, 100) == 0
+    need = L.chord_w4a16_grouped_workspace_bytes(8, 1024)
+    assert need >= 256 + (2 * 8 + 2) * 4 + (1024 // 8) * 4
+    # contiguous: E out of range, K % 64, SiLU with N % 64, small workspace, tcgen05 with N % 128
+    rc, msg = _rc_and_msg(L, L.chord_w4a16_grouped_gemm_contiguous(P, 1024, P, 0, 0, P, 256, 128, 0, P, None,
+                                                                   P, need, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "E=" in msg
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_grouped_gemm_contiguous(P, 1024, P, 8, 0, P, 256, 100, 0, P, None,
+                                                                 P, need, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_grouped_gemm_contiguous(P, 1024, P, 8, 0, P, 96, 128, 1, P, None,
+                                                                 P, need, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_grouped_gemm_contiguous(P, 1024, P, 8, 0, P, 256, 128, 0, P, None,
+                                                                 P, need - 1, None, None))
+    assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL
+    t = chord.chord_tuning(chord.CHORD_PATH_LARGE_M, 0, 0, 0)
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_grouped_gemm_contiguous(P, 1024, P, 8, 0, P, 192, 128, 0, P,
+                                                                 ctypes.byref(t), P, need, None, None))
+    assert rc == chord.CHORD_ERR_UNSUPPORTED
+    # masked: max_m % 16, E out of range, small workspace (rows = E * max_m)
+    rc, msg = _rc_and_msg(L, L.chord_w4a16_grouped_gemm_masked(P, P, 8, 24, 0, P, 256, 128, 0, P, None, P,
+                                                               need, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "max_m" in msg
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_grouped_gemm_masked(P, P, 2000, 32, 0, P, 256, 128, 0, P, None, P,
+                                                             need, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_grouped_gemm_masked(P, P, 8, 256, 0, P, 256, 128, 0, P, None, P,
+                                                             need, None, None))
+    assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(chord, "_lib", None)
     monkeypatch.setattr(chord, "LIB_PATH", str(tmp_path / "missing.so"))

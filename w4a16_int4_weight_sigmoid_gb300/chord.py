@@ -64,6 +64,10 @@ _SIGS = {
     "chord_moe_sum": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "chord_w4a16_gemm_workspace_bytes": (_Z, [_I]),
     "chord_w4a16_gemm": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P, _P]),
+    "chord_w4a16_grouped_workspace_bytes": (_Z, [_I, _Z]),
+    "chord_w4a16_grouped_gemm_contiguous": (_I, [_P, _Z, _P, _I, _I, _P, _I, _I, _I, _P, _P, _P, _Z,
+                                                 _P, _P]),
+    "chord_w4a16_grouped_gemm_masked": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _Z, _P, _P]),
     "chord_moe_layer_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "chord_moe_layer_plan": (_I, [_I, _I, _I, _P]),
     "chord_moe_layer": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z,
@@ -234,6 +238,32 @@ def chord_w4a16_gemm(A, packed_w, N: int, K: int, epilogue: int, C, workspace, t
         _ptr(A, None, "A"), _ptr(packed_w, torch.uint8, "packed_w"), N, K, A.shape[0], epilogue,
         _ptr(C, None, "C"), tun[0] if tun else None, _ptr(workspace, torch.uint8, "workspace"),
         workspace.numel(), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def chord_w4a16_grouped_workspace_bytes(E: int, rows: int) -> int:
+    return lib().chord_w4a16_grouped_workspace_bytes(E, rows)
+
+
+def chord_w4a16_grouped_gemm_contiguous(A, group_rows, packed_w, N: int, K: int, epilogue: int, C, workspace,
+                                        expected_m: int = 0, tuning=None, dev_status=None, stream=None):
+    """Contiguous layout: A [rows, K], expert groups in order, each padded to 128 rows."""
+    tun = _tuning(tuning)
+    _check(lib().chord_w4a16_grouped_gemm_contiguous(
+        _ptr(A, None, "A"), A.shape[0], _ptr(group_rows, torch.int32, "group_rows"), group_rows.numel(),
+        expected_m, _ptr(packed_w, torch.uint8, "packed_w"), N, K, epilogue, _ptr(C, None, "C"),
+        tun[0] if tun else None, _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def chord_w4a16_grouped_gemm_masked(A, group_rows, packed_w, N: int, K: int, epilogue: int, C, workspace,
+                                    expected_m: int = 0, tuning=None, dev_status=None, stream=None):
+    """Masked layout: A [E, max_m, K], the first group_rows[e] rows of expert e are used."""
+    tun = _tuning(tuning)
+    _check(lib().chord_w4a16_grouped_gemm_masked(
+        _ptr(A, None, "A"), _ptr(group_rows, torch.int32, "group_rows"), A.shape[0], A.shape[1], expected_m,
+        _ptr(packed_w, torch.uint8, "packed_w"), N, K, epilogue, _ptr(C, None, "C"),
+        tun[0] if tun else None, _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 
 def chord_moe_sum(y, topk_weights, sorted_positions, out, stream=None):

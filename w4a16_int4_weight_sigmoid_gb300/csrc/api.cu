@@ -378,6 +378,80 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
   return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "gemm launch");
 }
 
+}  // extern "C"
+
+namespace {
+
+// Grouped-layout GEMM: the block map from the per-expert row counts, then
+// the indexed GEMM on direct rows.  capacity = rows of A and C.
+int grouped_impl(const chord_bf16* A, size_t capacity, const int32_t* group_rows, int E, bool masked,
+                 int max_m, double tok_e, const void* packed_w, int N, int K, int epilogue, chord_bf16* C,
+                 const chord_tuning* tuning, void* workspace, size_t ws_bytes, int* dev_status, void* stream) {
+  int rc = check_tuning(tuning);
+  if (rc) return rc;
+  rc = check_gemm_shapes(N, K, epilogue);
+  if (rc) return rc;
+  if (E < 1 || E > 1024) return fail(CHORD_ERR_INVALID_ARG, "E=%d not in [1, 1024]", E);
+  if (capacity > 0x7fffffffu) return fail(CHORD_ERR_INVALID_ARG, "%zu rows: too many", capacity);
+  if (capacity == 0) return CHORD_OK;
+  if (!A || !group_rows || !packed_w || !C) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(A) || !aligned16(packed_w)) return fail(CHORD_ERR_INVALID_ARG, "A and packed_w must be 16-byte aligned");
+  if (!workspace || !aligned16(workspace)) return fail(CHORD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  const size_t need = chord_w4a16_grouped_workspace_bytes(E, capacity);
+  if (ws_bytes < need) return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "grouped GEMM workspace %zu < %zu", ws_bytes, need);
+  chord_tuning plan{};
+  if (tuning) plan = *tuning;
+  if (!plan.path) plan.path = (tok_e >= kLargeTokE && N % 128 == 0) ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
+  if (!plan.rows_per_pass) plan.rows_per_pass = rows_per_pass_for(tok_e);
+  if (plan.path == CHORD_PATH_LARGE_M && N % 128 != 0)   // checked before anything is launched
+    return fail(CHORD_ERR_UNSUPPORTED, "tcgen05 path needs N %% 128 == 0");
+  // BLOCK_M: 16 on the tcgen05 path; else one pass per block where the
+  // group size allows (every padded group is a multiple of BLOCK_M)
+  const int seg = masked ? max_m : 128;
+  int bm = 16;
+  if (plan.path != CHORD_PATH_LARGE_M) bm = seg % plan.rows_per_pass == 0 ? plan.rows_per_pass : (seg % 16 == 0 ? 16 : 8);
+  char* ws = static_cast<char*>(workspace);
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + kWorkBytes);
+  int32_t *counts = meta, *offsets = meta + E, *ntpp = meta + 2 * E + 1;
+  int32_t* eids = reinterpret_cast<int32_t*>(ws + kWorkBytes + round_up((2 * static_cast<size_t>(E) + 2) * 4, 256));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = chord::grouped_setup_launch(group_rows, E, masked, max_m, bm, static_cast<long long>(capacity),
+                                              counts, offsets, ntpp, eids, dev_status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "grouped setup launch");
+  return gemm_impl(A, 0, packed_w, E, N, K, static_cast<int>(capacity), 1, nullptr, eids, ntpp, counts, offsets, bm,
+                   capacity, epilogue, C, &plan, tok_e, ws, kWorkBytes, dev_status, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+// [256 B work counters | counts, offsets, ntpp | expert_ids for up to rows/8 blocks]
+size_t chord_w4a16_grouped_workspace_bytes(int E, size_t rows) {
+  if (E < 1 || E > 1024) return 0;
+  return kWorkBytes + round_up((2 * static_cast<size_t>(E) + 2) * 4, 256) + round_up((rows / 8 + 1) * 4, 256);
+}
+
+int chord_w4a16_grouped_gemm_contiguous(const chord_bf16* A, size_t a_rows, const int32_t* group_rows, int E,
+                                        int expected_m, const void* packed_w, int N, int K, int epilogue,
+                                        chord_bf16* C, const chord_tuning* tuning, void* workspace,
+                                        size_t ws_bytes, int* dev_status, void* stream) {
+  const double tok_e = expected_m > 0 ? expected_m : (E > 0 ? static_cast<double>(a_rows) / E : 0.0);
+  return grouped_impl(A, a_rows, group_rows, E, false, 0, tok_e, packed_w, N, K, epilogue, C, tuning, workspace,
+                      ws_bytes, dev_status, stream);
+}
+
+int chord_w4a16_grouped_gemm_masked(const chord_bf16* A, const int32_t* group_rows, int E, int max_m,
+                                    int expected_m, const void* packed_w, int N, int K, int epilogue,
+                                    chord_bf16* C, const chord_tuning* tuning, void* workspace, size_t ws_bytes,
+                                    int* dev_status, void* stream) {
+  if (max_m <= 0 || max_m % 16 != 0) return fail(CHORD_ERR_INVALID_ARG, "max_m=%d must be a positive multiple of 16", max_m);
+  if (E < 1 || E > 1024) return fail(CHORD_ERR_INVALID_ARG, "E=%d not in [1, 1024]", E);
+  const double tok_e = expected_m > 0 ? expected_m : max_m;
+  return grouped_impl(A, static_cast<size_t>(E) * max_m, group_rows, E, true, max_m, tok_e, packed_w, N, K,
+                      epilogue, C, tuning, workspace, ws_bytes, dev_status, stream);
+}
+
 size_t chord_w4a16_moe_gemm_workspace_bytes(size_t capacity, int K, int a_gather) {
   return kWorkBytes + (a_gather ? capacity * static_cast<size_t>(K > 0 ? K : 0) * 2 : 0);
 }

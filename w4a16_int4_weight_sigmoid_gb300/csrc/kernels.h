@@ -59,6 +59,13 @@ struct GemmLaunch {
 // Dense GEMM: one-expert block map (counts, offsets, ntpp, expert_ids) for M rows.
 cudaError_t dense_setup_launch(int M, int bm, int32_t* counts, int32_t* offsets, int32_t* ntpp,
                                int32_t* expert_ids, cudaStream_t st);
+// Grouped layouts: block map from per-expert row counts (one CTA, E <= 1024).
+// masked: group g at rows [g*max_m, g*max_m + rows); contiguous: groups in
+// order, each padded to 128 rows.  A bad count or a total above capacity
+// records CHORD_ERR_INVALID_ARG and leaves an empty map.
+cudaError_t grouped_setup_launch(const int32_t* group_rows, int E, bool masked, int max_m, int bm,
+                                 long long capacity, int32_t* counts, int32_t* offsets, int32_t* ntpp,
+                                 int32_t* expert_ids, int* status, cudaStream_t st);
 cudaError_t gemm_small_launch(const GemmLaunch& g, int rows_per_pass, cudaStream_t st);
 size_t gemm_large_smem_bytes();
 cudaError_t gemm_large_launch(const GemmLaunch& g, const uint16_t* B, size_t b_rows, cudaStream_t st);
