@@ -67,9 +67,10 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--cpu-budget-s", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--report", choices=["route_align", "m_sweep"], default=None,
+    p.add_argument("--report", choices=["route_align", "m_sweep", "grouped"], default=None,
                    help="report-only measurements instead of the headline line: router+align "
-                        "microseconds per (M, BLOCK_M), or the layer over M = 1..8192 at EP8 shapes")
+                        "microseconds per (M, BLOCK_M), the layer over M = 1..8192 at EP8 shapes, "
+                        "or the grouped-layout GEMMs at EP8 expert shapes")
     return p.parse_args()
 
 
@@ -596,6 +597,48 @@ def run_report(args):
                              "route_then_align_us": round(graph_us([route, align]), 2),
                              "chord_moe_route_align_us": round(graph_us([fused]), 2)})
         note = "CUDA graph of 20 back-to-back passes, median of 30 replays; 384 experts, top-8, all local"
+    elif args.report == "grouped":
+        # the grouped layouts at the pages' scenarios, Kimi EP8 expert shapes:
+        # masked decode with 32 tokens per expert, contiguous prefill with 128
+        base = wl.EP8_DECODE
+        E, H, I = base.E_local, base.H, base.I
+        d = wl.layer_inputs(wl.LayerShape("grouped", 64, H, I, base.E_total, E, 0, base.topk, base.seed))
+        layer = W4A16MoELayer(d["w13_q"], d["w13_s"], d["w2_q"], d["w2_s"], base.E_total, 0, base.topk,
+                              device=dev)
+        del d
+        peaks, _ = load_peaks()
+        wbytes = {"gate_up": E * (2 * I * H // 2 + 2 * I * (H // 32) * 2), "down": E * (H * I // 2 + H * (I // 32) * 2)}
+        for layout, per_e in (("masked", 32), ("contiguous", 128)):
+            rows_n = E * per_e
+            g = torch.full((E,), per_e, dtype=torch.int32, device=dev)
+            x = to_device(wl.activations(rows_n, H, 81), dev)
+            h = torch.empty((rows_n, I), dtype=torch.bfloat16, device=dev)
+            y = torch.empty((rows_n, H), dtype=torch.bfloat16, device=dev)
+            ws = torch.zeros(chord.chord_w4a16_grouped_workspace_bytes(E, rows_n), dtype=torch.uint8, device=dev)
+            st = torch.zeros(1, dtype=torch.int32, device=dev)
+            for name, A, W, N, K, epi, C in (("gate_up", x, layer.w13, 2 * I, H, chord.CHORD_EPI_SILU_MUL, h),
+                                             ("down", h, layer.w2, H, I, chord.CHORD_EPI_STORE, y)):
+                if layout == "masked":
+                    f = lambda A=A, W=W, N=N, K=K, epi=epi, C=C: chord.chord_w4a16_grouped_gemm_masked(
+                        A.view(E, per_e, K), g, W, N, K, epi, C.view(E, per_e, -1), ws, per_e, dev_status=st)
+                else:
+                    f = lambda A=A, W=W, N=N, K=K, epi=epi, C=C: chord.chord_w4a16_grouped_gemm_contiguous(
+                        A, g, W, N, K, epi, C, ws, per_e, dev_status=st)
+                us = graph_us([f], reps_in_graph=10, replays=20)
+                byts = wbytes[name] + rows_n * K * 2 + rows_n * (N // 2 if epi == chord.CHORD_EPI_SILU_MUL else N) * 2
+                flops = 2.0 * rows_n * N * K
+                t_hbm, t_tc = byts / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops_sustained"] * 1e12)
+                bound = "hbm" if t_hbm >= t_tc else "tensor"
+                rows.append({"layout": layout, "rows_per_expert": per_e, "gemm": name, "us": round(us, 2),
+                             "bound": bound, "frac": round(max(t_hbm, t_tc) / (us * 1e-6), 4),
+                             "achieved": round(byts / (us * 1e-6) / 1e9, 1) if bound == "hbm"
+                             else round(flops / (us * 1e-6) / 1e12, 1),
+                             "unit": "GB/s" if bound == "hbm" else "TFLOP/s"})
+            torch.cuda.synchronize()
+            assert st.item() == 0, f"device status {st.item()}"
+        note = ("grouped-layout GEMMs, 48 experts of Kimi EP8 shapes (H 7168, I 2048), every expert's weights "
+                "touched; CUDA graph of 10 back-to-back calls, median of 20 replays; frac against the measured "
+                "HBM rate or sustained BF16 rate, whichever bounds")
     else:
         base = wl.EP8_DECODE
         d = wl.layer_inputs(wl.LayerShape("m_sweep", 8192, base.H, base.I, base.E_total, base.E_local,
@@ -625,8 +668,8 @@ def run_report(args):
             M *= 2
         note = ("one layer, chord_moe_layer, EP8 shapes (H 7168, I 2048, 48 of 384 experts, top-8), "
                 "the first M tokens of one seeded 8192-token draw; CUDA graph of back-to-back calls")
-    if torch.cuda.is_available():
-        assert int(layer.dev_status.item() if args.report == "m_sweep" else 0) == 0
+    if torch.cuda.is_available() and args.report == "m_sweep":
+        assert int(layer.dev_status.item()) == 0
     print(json.dumps({"report": args.report, "unit": "us", "note": note, "rows": rows}))
 
 
