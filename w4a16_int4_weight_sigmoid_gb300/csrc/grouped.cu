@@ -20,16 +20,18 @@ constexpr int kSetupThreads = 1024;   // one thread per expert (E <= 1024)
 __global__ void __launch_bounds__(kSetupThreads) grouped_setup_kernel(
     const int32_t* __restrict__ group_rows, int E, int masked, int max_m, int bm, long long capacity,
     int32_t* counts, int32_t* offsets, int32_t* ntpp, int32_t* expert_ids, int* status) {
-  __shared__ int s_off[kSetupThreads + 1];
-  __shared__ int s_warp[kSetupThreads / 32];
+  // 64-bit sizes and sums: a count is at most the rows of A (< 2^31), so
+  // no padded size or partial sum can wrap before it is checked
+  __shared__ long long s_off[kSetupThreads + 1];
+  __shared__ long long s_warp[kSetupThreads / 32];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) s_bad = 0;
   __syncthreads();
-  int c = 0, p = 0;
+  long long c = 0, p = 0;
   if (tid < E) {
     c = group_rows[tid];
-    const int limit = masked ? max_m : 0x7fffffff;
+    const long long limit = masked ? max_m : capacity;
     if (c < 0 || c > limit) {
       s_bad = 1;
       c = 0;
@@ -37,25 +39,25 @@ __global__ void __launch_bounds__(kSetupThreads) grouped_setup_kernel(
     p = masked ? max_m : (c + 127) / 128 * 128;
   }
   // exclusive scan of the padded group sizes over the experts
-  int v = p;
+  long long v = p;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, v, d);
+    const long long o = __shfl_up_sync(0xffffffffu, v, d);
     if (lane >= d) v += o;
   }
   if (lane == 31) s_warp[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    int w = s_warp[lane];
+    long long w = s_warp[lane];
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, w, d);
+      const long long o = __shfl_up_sync(0xffffffffu, w, d);
       if (lane >= d) w += o;
     }
     s_warp[lane] = w;   // inclusive over warps
   }
   __syncthreads();
-  const int excl = v - p + (warp > 0 ? s_warp[warp - 1] : 0);
+  const long long excl = v - p + (warp > 0 ? s_warp[warp - 1] : 0);
   if (tid < E) s_off[tid] = excl;
   if (tid == E - 1) s_off[E] = excl + p;
   __syncthreads();
@@ -63,9 +65,9 @@ __global__ void __launch_bounds__(kSetupThreads) grouped_setup_kernel(
   if (total > capacity) s_bad = 1;
   __syncthreads();
   const bool bad = s_bad != 0;
-  if (tid < E) {
-    counts[tid] = bad ? 0 : c;
-    offsets[tid] = bad ? 0 : s_off[tid];
+  if (tid < E) {   // capacity < 2^31, so every value written fits an int
+    counts[tid] = bad ? 0 : static_cast<int>(c);
+    offsets[tid] = bad ? 0 : static_cast<int>(s_off[tid]);
   }
   const int used = bad ? 0 : static_cast<int>(total);
   if (tid == 0) {
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(kSetupThreads) grouped_setup_kernel(
   // (every padded group size is a multiple of bm)
   const int nblk = used / bm;
   for (int b = tid; b < nblk; b += kSetupThreads) {
-    const int row = b * bm;
+    const long long row = static_cast<long long>(b) * bm;
     int lo = 0, hi = E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
