@@ -216,6 +216,12 @@ int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E,
  * token activations [M, K]) and row(r) = r when a_gather = 0 (A = rows in
  * sorted order [capacity, K], e.g. the gate/up output).
  *   block_m  the BLOCK_M the align buffers were built with
+ *   align buffers  as chord_moe_align writes them for this M, topk and
+ *            block_m: expert_offsets[e] + expert_counts[e] <= capacity, and
+ *            sorted_token_ids below M*topk on every counted row.  The kernels
+ *            range-check the block count and the expert ids (recording
+ *            CHORD_ERR_INVALID_ARG / CHORD_ERR_ROUTING_INVALID) but do not
+ *            re-check every row index against these buffers.
  *   C        BF16 [capacity, N] (STORE) or [capacity, N/2] (SILU_MUL); padding
  *            rows are not written
  *   workspace  chord_w4a16_moe_gemm_workspace_bytes() bytes, 16-byte aligned.
