@@ -516,12 +516,12 @@ namespace {
 // chord_moe_sum with a choice of programmatic launch (pdl: may start before
 // the down GEMM ends and waits for it).
 int moe_sum_impl(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions, int M,
-                 int topk, int H, chord_bf16* out, void* stream, bool pdl) {
+                 int topk, int H, chord_bf16* out, void* stream, bool pdl, int y_rows = 0x7fffffff) {
   if (M < 0 || topk < 1 || H <= 0 || H % 8 != 0) return fail(CHORD_ERR_INVALID_ARG, "bad M/topk/H (H %% 8 == 0)");
   if (M > 0 && (!y || !topk_weights || !sorted_positions || !out)) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(y) || !aligned16(out)) return fail(CHORD_ERR_INVALID_ARG, "y and out must be 16-byte aligned");
   cudaError_t e = chord::moe_sum_launch(y, topk_weights, sorted_positions, M, topk, H, out,
-                                        static_cast<cudaStream_t>(stream), pdl);
+                                        static_cast<cudaStream_t>(stream), pdl, y_rows);
   return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "moe_sum launch");
 }
 
@@ -613,7 +613,7 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
                  w.cap, CHORD_EPI_STORE, y, &plan, tok_e, ws + w.work, kWorkBytes, dev_status, stream,
                  pdl ? 2 : 0);
   if (rc) return rc;
-  return moe_sum_impl(y, tw, pos, M, topk, H, out, stream, pdl);
+  return moe_sum_impl(y, tw, pos, M, topk, H, out, stream, pdl, static_cast<int>(w.cap));
 }
 
 }  // extern "C"

@@ -73,6 +73,7 @@ cudaError_t gather_rows_launch(const uint16_t* x, const int32_t* sorted, const i
                                int sentinel, int K, size_t capacity, uint16_t* out, cudaStream_t st);
 
 cudaError_t moe_sum_launch(const uint16_t* y, const float* w, const int32_t* pos, int M, int topk,
-                           int H, uint16_t* out, cudaStream_t st, bool pdl = false);
+                           int H, uint16_t* out, cudaStream_t st, bool pdl = false,
+                           int y_rows = 0x7fffffff);
 
 }  // namespace chord

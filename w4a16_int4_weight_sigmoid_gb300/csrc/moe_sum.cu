@@ -13,9 +13,11 @@ constexpr int kColsPerCta = kThreads * 8;
 // kOrdered: a programmatic launch; y, w and pos come from kernels that may
 // still be running when this grid starts, so they are read after the wait
 // with ordered L2 loads (see grid_dep_wait), not through the read-only cache.
+// A position at or past y_rows counts as no assignment, so a position map
+// that a failed earlier kernel left unwritten cannot send a load out of y.
 template <bool kOrdered>
 __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* y, const float* w,
-                                                           const int32_t* pos, int topk, int H,
+                                                           const int32_t* pos, int topk, int H, int y_rows,
                                                            uint16_t* __restrict__ out) {
   grid_dep_wait();
   grid_dep_launch();
@@ -35,6 +37,7 @@ __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* y, co
       const bool in = j0 + j < topk;
       const size_t o = static_cast<size_t>(t) * topk + (in ? j0 + j : 0);
       p[j] = in ? (kOrdered ? ld_cg(pos + o) : __ldg(pos + o)) : -1;
+      if (p[j] >= y_rows) p[j] = -1;
       wj[j] = in ? (kOrdered ? ld_cg(w + o) : __ldg(w + o)) : 0.f;
     }
     uint4 v[8];
@@ -67,11 +70,12 @@ __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* y, co
 }  // namespace
 
 cudaError_t moe_sum_launch(const uint16_t* y, const float* w, const int32_t* pos, int M, int topk,
-                           int H, uint16_t* out, cudaStream_t st, bool pdl) {
+                           int H, uint16_t* out, cudaStream_t st, bool pdl, int y_rows) {
   if (M == 0) return cudaSuccess;
   dim3 grid(M, (H + kColsPerCta - 1) / kColsPerCta);
-  if (pdl) return launch_kernel(moe_sum_kernel<true>, grid, dim3(kThreads), 0, st, true, y, w, pos, topk, H, out);
-  return launch_kernel(moe_sum_kernel<false>, grid, dim3(kThreads), 0, st, false, y, w, pos, topk, H, out);
+  if (pdl)
+    return launch_kernel(moe_sum_kernel<true>, grid, dim3(kThreads), 0, st, true, y, w, pos, topk, H, y_rows, out);
+  return launch_kernel(moe_sum_kernel<false>, grid, dim3(kThreads), 0, st, false, y, w, pos, topk, H, y_rows, out);
 }
 
 }  // namespace chord
