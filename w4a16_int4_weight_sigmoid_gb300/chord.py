@@ -247,6 +247,8 @@ def chord_w4a16_grouped_workspace_bytes(E: int, rows: int) -> int:
 def chord_w4a16_grouped_gemm_contiguous(A, group_rows, packed_w, N: int, K: int, epilogue: int, C, workspace,
                                         expected_m: int = 0, tuning=None, dev_status=None, stream=None):
     """Contiguous layout: A [rows, K], expert groups in order, each padded to 128 rows."""
+    if A.dim() != 2:
+        raise ValueError("contiguous layout: A must be [rows, K]")
     tun = _tuning(tuning)
     _check(lib().chord_w4a16_grouped_gemm_contiguous(
         _ptr(A, None, "A"), A.shape[0], _ptr(group_rows, torch.int32, "group_rows"), group_rows.numel(),
@@ -258,6 +260,8 @@ def chord_w4a16_grouped_gemm_contiguous(A, group_rows, packed_w, N: int, K: int,
 def chord_w4a16_grouped_gemm_masked(A, group_rows, packed_w, N: int, K: int, epilogue: int, C, workspace,
                                     expected_m: int = 0, tuning=None, dev_status=None, stream=None):
     """Masked layout: A [E, max_m, K], the first group_rows[e] rows of expert e are used."""
+    if A.dim() != 3 or group_rows.numel() != A.shape[0]:
+        raise ValueError("masked layout: A must be [E, max_m, K] with one group_rows entry per expert")
     tun = _tuning(tuning)
     _check(lib().chord_w4a16_grouped_gemm_masked(
         _ptr(A, None, "A"), _ptr(group_rows, torch.int32, "group_rows"), A.shape[0], A.shape[1], expected_m,
