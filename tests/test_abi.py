@@ -194,6 +194,17 @@ def test_grouped_entry_points_reject_before_launch(L):
     assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_grouped_wrappers_check_shapes_before_the_library():
+    """A masked call whose group counts do not match A's experts, or a
+    contiguous call with a 3-D A, is refused by the binding itself."""
+    import torch
+    A3 = torch.zeros((2, 16, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="one group_rows entry per expert"):
+        chord.chord_w4a16_grouped_gemm_masked(A3, torch.zeros(3, dtype=torch.int32), None, 64, 64, 0, None, None)
+    with pytest.raises(ValueError, match="rows, K"):
+        chord.chord_w4a16_grouped_gemm_contiguous(A3, torch.zeros(2, dtype=torch.int32), None, 64, 64, 0, None, None)
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(chord, "_lib", None)
     monkeypatch.setattr(chord, "LIB_PATH", str(tmp_path / "missing.so"))
