@@ -18,6 +18,13 @@ come from a second CUDA-event-timed region of K steps that runs the same
 layer as four graph replays (route+align, gate/up, down, combine: the
 layer's C-ABI calls one by one) with events between them.
 
+The JSON line's headline (`value`, `roofline`, ...) is the selected workload
+(default EP8 decode); unless --only is given, `workloads` carries the same
+fields for the metric's other layer shards, measured the same way in the same
+run: the TP8 decode shard (HBM-bound, GB/s) and the EP8 prefill shard
+(tensor-bound, TFLOP/s against the measured BF16 peak: the burst figure when
+the timed region lasts under a second, else the sustained one).
+
 `e2e` repeats the measurement through the public single call
 (chord_moe_layer) with pinned HOST inputs and outputs: each step copies x
 and the router logits host->device and the layer output device->host.
@@ -67,6 +74,9 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--cpu-budget-s", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--only", action="store_true",
+                   help="measure the selected workload only (by default the line also carries the "
+                        "metric's other layer workloads under 'workloads')")
     p.add_argument("--report", choices=["route_align", "m_sweep", "grouped"], default=None,
                    help="report-only measurements instead of the headline line: router+align "
                         "microseconds per (M, BLOCK_M), the layer over M = 1..8192 at EP8 shapes, "
@@ -302,27 +312,26 @@ def algorithmic(shape, touched, rows):
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, world, rank, local):
-    import torch
-    from w4a16_int4_weight_sigmoid_gb300 import build as B
-    from w4a16_int4_weight_sigmoid_gb300 import chord
-    from w4a16_int4_weight_sigmoid_gb300 import workload as wl
+def peak_for(peaks, region_s):
+    """BF16 peak for a tensor-bound kernel: the burst figure for a region
+    shorter than a second (the kernel runs at its unthrottled clock), the
+    sustained one for a longer region."""
+    if region_s < 1.0:
+        return peaks["bf16_tflops"], "burst"
+    return peaks["bf16_tflops_sustained"], "sustained"
 
-    B.build()
-    chord.lib()
-    torch.cuda.set_device(local)
+
+def measure_workload(shape, steps, warmup, R, world, rank, local, seed_base, e2e_steps, sampler_uuid):
+    """Time one layer workload: K layer-graph replays (the step), then the
+    same K steps as the layer's C-ABI calls one by one for kernel durations,
+    then the public call with host copies (e2e).  Returns the fields of its
+    JSON entry (and replica 0 for the CPU baseline)."""
+    import torch
     device = f"cuda:{local}"
-    shape = wl.WORKLOADS[args.workload]
-    decode = shape.M * shape.topk / shape.E_total < 64
-    steps = args.steps if args.steps is not None else (20000 if decode else 300)
-    warmup = max(3, args.warmup if args.warmup is not None else (200 if decode else 10))
-    R = max(1, args.replicas)
-    reps = [Replica(shape, shape.seed + 1000 * r + 7919 * rank, device, keep_host=(r == 0))
+    reps = [Replica(shape, seed_base + 1000 * r + 7919 * rank, device, keep_host=(r == 0))
             for r in range(R)]
     for r in reps:
         r.capture()
-
-    # warm-up
     for i in range(warmup):
         reps[i % R].layer_graph.replay()
         for g in reps[i % R].graphs:
@@ -336,14 +345,7 @@ def run_ours(args, world, rank, local):
     nev = 5
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(local).uuid)
-        if uuid and not uuid.startswith("GPU-"):
-            uuid = "GPU-" + uuid
-    except Exception:
-        uuid = None
-    sampler = ClockSampler(uuid)
+    sampler = ClockSampler(sampler_uuid)
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
@@ -392,32 +394,37 @@ def run_ours(args, world, rank, local):
                 alg[k][q] += a[k][q] / steps
 
     peaks, peak_src = load_peaks()
+    bf16_peak, peak_kind = peak_for(peaks, staged_ms / 1e3)
+    src = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     dom = max(("gate_up", "down"), key=lambda n: kern_us[n])
-    t_s = kern_us[dom] * 1e-6
-    t_hbm = alg[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = alg[dom]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12)
-    if t_hbm >= t_tc:
-        ach = alg[dom]["bytes"] / t_s / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        ach = alg[dom]["flops"] / t_s / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = committed_traffic(dom, shape.name, "large" if reps[0].large else "small")
-    roof["kernel"] = f"{'gemm_large (tcgen05)' if reps[0].large else 'gemm_small'} ({dom})"
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
-    roof["algorithmic_bytes_per_launch"] = alg[dom]["bytes"]
-    roof["algorithmic_flops_per_launch"] = alg[dom]["flops"]
+    roofs = {}
+    for kname in ("gate_up", "down"):
+        t_s = kern_us[kname] * 1e-6
+        t_hbm = alg[kname]["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        t_tc = alg[kname]["flops"] / (bf16_peak * 1e12)
+        if t_hbm >= t_tc:
+            ach = alg[kname]["bytes"] / t_s / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "peak_source": f"{src}, hbm_gbs"}
+        else:
+            ach = alg[kname]["flops"] / t_s / 1e12
+            roof = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s",
+                    "peak_source": f"{src}, bf16 {peak_kind} (timed region {staged_ms / 1e3:.3f} s)"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["traffic"] = committed_traffic(kname, shape.name, "large" if reps[0].large else "small")
+        roof["kernel"] = f"{'gemm_large (tcgen05)' if reps[0].large else 'gemm_small'} ({kname})"
+        roof["algorithmic_bytes_per_launch"] = alg[kname]["bytes"]
+        roof["algorithmic_flops_per_launch"] = alg[kname]["flops"]
+        roofs[kname] = roof
 
-    # whole-layer roofline: slower of bytes at HBM peak and FLOPs at BF16 peak
+    # whole-layer roofline: slower of bytes at HBM peak and FLOPs at the BF16 peak
     lay_bytes = alg["gate_up"]["bytes"] + alg["down"]["bytes"]
     lay_flops = alg["gate_up"]["flops"] + alg["down"]["flops"]
-    t_lay_min = max(lay_bytes / (peaks["hbm_gbs"] * 1e9), lay_flops / (peaks["bf16_tflops_sustained"] * 1e12))
+    t_lay_min = max(lay_bytes / (peaks["hbm_gbs"] * 1e9), lay_flops / (bf16_peak * 1e12))
     ms_per_step = elapsed_ms / steps
     value = shape.M * steps * world / (elapsed_ms / 1e3)
 
     # ----------------------------------------------------------- e2e
-    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, steps // 10)
     outs_pinned = [torch.empty((shape.M, shape.H), dtype=torch.bfloat16).pin_memory() for _ in range(R)]
     for i in range(max(3, R)):   # warm the whole path, copies included, on every replica
         r = reps[i % R]
@@ -445,37 +452,91 @@ def run_ours(args, world, rank, local):
     e2e = {"value": shape.M * e2e_steps * world / (e2e_ms / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
            "api": "chord_moe_layer"}
+    for r in reps:
+        assert r.status.item() == 0 and r.layer.dev_status.item() == 0, "device status after timing"
 
     launches_per_step = reps[0].layer_launches
     staged_launches = reps[0].align_launches + reps[0].gemm_launches + 2   # + route, combine
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
-        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    fields = {
+        "value": value, "unit": "tokens/s", "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
         "config": {"workload": shape.name, "M": shape.M, "H": shape.H, "I": shape.I,
                    "E_total": shape.E_total, "E_local": shape.E_local, "topk": shape.topk,
                    "weights": "INT4 group-32 symmetric, BF16 scales; BF16 activations",
                    "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {R} rotating layer replicas, each step's touched "
+                   "l2": f"inputs larger than L2: {R} rotating layer replica(s), each step's touched "
                          f"weights ~{alg['gate_up']['bytes'] / 1e6 + alg['down']['bytes'] / 1e6:.0f} MB "
                          f"> 129 MB L2",
-                   "touched_experts_per_replica": [s[0] for s in st],
-                   "local_rows_per_replica": [s[1] for s in st]},
+                   "touched_experts_per_replica": [x[0] for x in st],
+                   "local_rows_per_replica": [x[1] for x in st]},
         "e2e": e2e,
         "gpu_launches": launches_per_step * steps,
-        "step": "one chord_moe_layer call (CUDA graph replay; kernels chained by programmatic launches)",
         "kernel_timing": {"how": "second timed region of the same steps as the layer's C-ABI calls one "
                                  "by one (four graph replays, CUDA events between them)",
                           "steps": steps, "ms_per_step": staged_ms / steps,
                           "gpu_launches": staged_launches * steps},
-        "roofline": roof,
+        "roofline": roofs[dom],
+        "roofline_per_gemm": roofs,
         "layer_roofline": {"bytes": lay_bytes, "flops": lay_flops, "t_min_us": t_lay_min * 1e6,
-                           "t_us": ms_per_step * 1e3, "frac": t_lay_min / (ms_per_step * 1e-3)},
+                           "t_us": ms_per_step * 1e3, "frac": t_lay_min / (ms_per_step * 1e-3),
+                           "bf16_peak": f"{peak_kind} {bf16_peak} TFLOP/s"},
         "kernels_us": kern_us,
         "clocks": clocks,
     }
+    host = reps[0].host
+    del reps
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return fields, host
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from w4a16_int4_weight_sigmoid_gb300 import build as B
+    from w4a16_int4_weight_sigmoid_gb300 import chord
+    from w4a16_int4_weight_sigmoid_gb300 import workload as wl
+
+    B.build()
+    chord.lib()
+    torch.cuda.set_device(local)
+    shape = wl.WORKLOADS[args.workload]
+    decode = shape.M * shape.topk / shape.E_total < 64
+    steps = args.steps if args.steps is not None else (20000 if decode else 300)
+    warmup = max(3, args.warmup if args.warmup is not None else (200 if decode else 10))
+    R = max(1, args.replicas)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        if uuid and not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, steps // 10)
+    head, host = measure_workload(shape, steps, warmup, R, world, rank, local, shape.seed, e2e_steps, uuid)
+    line = {"metric": METRIC, "value": head.pop("value"), "unit": head.pop("unit"), "n_gpus": world,
+            "steps": head.pop("steps"), "warmup": head.pop("warmup"), "ms_per_step": head.pop("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", **head,
+            "step": "one chord_moe_layer call (CUDA graph replay; kernels chained by programmatic launches)"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(shape, reps[0].host, args.cpu_budget_s)
+        line["cpu_baseline"] = cpu_baseline(shape, host, args.cpu_budget_s)
+    del host
+    # the metric's other layer workloads, same steps, in the same line: the
+    # TP8 decode shard (HBM GB/s) and the EP8 prefill shard (TFLOPS)
+    if not args.only:
+        extra = {}
+        for other in wl.LAYER_WORKLOADS:
+            if other.name == shape.name:
+                continue
+            o_decode = other.M * other.topk / other.E_total < 64
+            o_R = 2 if o_decode else 1
+            o_steps = max(steps, 20)
+            o_e2e = max(3, o_steps // 10)
+            fields, h = measure_workload(other, o_steps, warmup, o_R, world, rank, local, other.seed, o_e2e, uuid)
+            del h
+            fields["tokens_per_s"] = fields.pop("value")
+            fields.pop("unit")
+            extra[other.name] = fields
+        line["workloads"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
 

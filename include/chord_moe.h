@@ -169,9 +169,10 @@ int chord_moe_route_align(const float* logits, const float* bias, int M, int E_t
  *   E_local <= CHORD_ALIGN_NOALLOC_MAX_EXPERTS; larger calls return
  *   CHORD_ERR_INVALID_ARG and launch nothing.
  *   Set-up: the first call on each device looks up the array's device
- *   address (cudaGetSymbolAddress) with that device current; make that first
- *   call before any stream capture.  It allocates nothing and calls no
- *   cudaMalloc/cudaFree.
+ *   address (cudaGetSymbolAddress) with that device current; under lazy
+ *   module loading that lookup may be what loads the library's module and
+ *   reserves the array.  Make that first call before any stream capture.  It
+ *   allocates nothing and calls no cudaMalloc/cudaFree.
  *   Sharing: all calls use the same array and it keeps the last call's
  *   contents (every call rewrites what it reads, so nothing needs clearing);
  *   calls whose executions overlap on the GPU (other streams, other threads)
@@ -226,8 +227,9 @@ int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E,
  *            rows are not written
  *   workspace  chord_w4a16_moe_gemm_workspace_bytes() bytes, 16-byte aligned.
  *            Its first 256 bytes are work-queue counters: zero them once when
- *            the workspace is allocated; every call leaves them zero (a call
- *            that stops on a device timeout may not).  With a_gather = 1 the
+ *            the workspace is allocated; every call leaves them zero (the
+ *            last CTA of each launch resets them, also after a device
+ *            timeout).  With a_gather = 1 the
  *            tensor-core path also stages the gathered rows there.
  *   dev_status  device int for errors found on the device (may be NULL)
  * Two paths ([Humming] "워크로드별 튜닝 및 JIT 컴파일": async-copy + MMA at

@@ -205,6 +205,56 @@ def test_grouped_wrappers_check_shapes_before_the_library():
         chord.chord_w4a16_grouped_gemm_contiguous(A3, torch.zeros(2, dtype=torch.int32), None, 64, 64, 0, None, None)
 
 
+def test_gemm_wrappers_check_operands_before_the_library():
+    """The C ABI sees raw pointers only, so the binding checks what it cannot:
+    BF16 operands, A's last dimension = K, and C large enough for N (STORE) or
+    N/2 (SiLU*mul) columns on every row.  Each mismatch raises ValueError
+    before any pointer is taken (these tensors are on the CPU)."""
+    import torch
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    STORE, SILU = chord.CHORD_EPI_STORE, chord.CHORD_EPI_SILU_MUL
+    A = torch.zeros((8, 64), dtype=bf)
+    # dense
+    with pytest.raises(ValueError, match="bfloat16"):
+        chord.chord_w4a16_gemm(A.float(), None, 64, 64, STORE, torch.zeros((8, 64), dtype=bf), None)
+    with pytest.raises(ValueError, match="bfloat16"):
+        chord.chord_w4a16_gemm(A, None, 64, 64, STORE, torch.zeros((8, 64), dtype=f32), None)
+    with pytest.raises(ValueError, match="last dimension"):
+        chord.chord_w4a16_gemm(A, None, 64, 128, STORE, torch.zeros((8, 64), dtype=bf), None)
+    with pytest.raises(ValueError, match="C's last dimension"):
+        chord.chord_w4a16_gemm(A, None, 64, 64, SILU, torch.zeros((8, 64), dtype=bf), None)
+    with pytest.raises(ValueError, match="same rows"):
+        chord.chord_w4a16_gemm(A, None, 64, 64, STORE, torch.zeros((4, 64), dtype=bf), None)
+    # contiguous
+    g2 = torch.zeros(2, dtype=i32)
+    with pytest.raises(ValueError, match="rows of A"):
+        chord.chord_w4a16_grouped_gemm_contiguous(A, g2, None, 64, 64, STORE, torch.zeros((7, 64), dtype=bf), None)
+    with pytest.raises(ValueError, match="last dimension"):
+        chord.chord_w4a16_grouped_gemm_contiguous(A, g2, None, 64, 128, STORE, torch.zeros((8, 64), dtype=bf), None)
+    with pytest.raises(ValueError, match="C's last dimension"):
+        chord.chord_w4a16_grouped_gemm_contiguous(A, g2, None, 128, 64, STORE, torch.zeros((8, 64), dtype=bf), None)
+    # masked
+    A3 = torch.zeros((2, 16, 64), dtype=bf)
+    with pytest.raises(ValueError, match="experts and rows"):
+        chord.chord_w4a16_grouped_gemm_masked(A3, g2, None, 64, 64, STORE, torch.zeros((2, 8, 64), dtype=bf), None)
+    with pytest.raises(ValueError, match="bfloat16"):
+        chord.chord_w4a16_grouped_gemm_masked(A3, g2, None, 64, 64, STORE, torch.zeros((2, 16, 64), dtype=f32), None)
+    with pytest.raises(ValueError, match="C's last dimension"):
+        chord.chord_w4a16_grouped_gemm_masked(A3, g2, None, 128, 64, SILU, torch.zeros((2, 16, 32), dtype=bf), None)
+    # indexed: gathered A needs M token rows, C needs capacity rows
+    st = torch.zeros(48, dtype=i32)
+    e = torch.zeros(3, dtype=i32)
+    with pytest.raises(ValueError, match="A holds"):
+        chord.chord_w4a16_moe_gemm(A, True, None, 2, 64, 64, 16, 2, st, e, e, e, e, 16, STORE,
+                                   torch.zeros((48, 64), dtype=bf), None)
+    with pytest.raises(ValueError, match="C holds"):
+        chord.chord_w4a16_moe_gemm(A, True, None, 2, 64, 64, 8, 2, st, e, e, e, e, 16, STORE,
+                                   torch.zeros((40, 64), dtype=bf), None)
+    with pytest.raises(ValueError, match="A holds"):
+        chord.chord_w4a16_moe_gemm(A, False, None, 2, 64, 64, 8, 2, st, e, e, e, e, 16, STORE,
+                                   torch.zeros((48, 64), dtype=bf), None)
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(chord, "_lib", None)
     monkeypatch.setattr(chord, "LIB_PATH", str(tmp_path / "missing.so"))

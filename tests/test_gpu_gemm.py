@@ -131,7 +131,8 @@ def test_gemm_direct_rows_and_header_check(path):
     assert status.item() == chord.CHORD_ERR_PREPACK_MISMATCH
     # a plain blob used for SiLU*mul is refused too
     status.zero_()
-    _run_gemm(to_device(A), False, packed, E, N, K, M, topk, up, bm, SILU, C, path, status)
+    C_half = torch.zeros((cap, N // 2), dtype=torch.bfloat16, device="cuda")
+    _run_gemm(to_device(A), False, packed, E, N, K, M, topk, up, bm, SILU, C_half, path, status)
     assert status.item() == chord.CHORD_ERR_PREPACK_MISMATCH
 
 

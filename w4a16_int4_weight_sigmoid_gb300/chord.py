@@ -112,6 +112,27 @@ def _ptr(t, dtype=None, name="tensor"):
     return t.data_ptr()
 
 
+def _check_operands(A, C, K: int, N: int, epilogue: int, a_rows: int, c_rows: int, what: str):
+    """Shape and dtype checks the C ABI cannot make (it sees raw pointers):
+    A holds a_rows rows of K BF16 values and C holds c_rows rows of N (STORE)
+    or N/2 (SiLU*mul) BF16 values.  Raises ValueError before anything runs."""
+    for name, t in (("A", A), ("C", C)):
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{what}: {name} must be a torch.Tensor")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{what}: {name} must be bfloat16, got {t.dtype}")
+    if A.shape[-1] != K:
+        raise ValueError(f"{what}: A's last dimension {A.shape[-1]} != K={K}")
+    if A.numel() < a_rows * K:
+        raise ValueError(f"{what}: A holds {A.numel()} values, needs {a_rows} rows of K={K}")
+    ncols = N // 2 if epilogue == CHORD_EPI_SILU_MUL else N
+    if C.shape[-1] != ncols:
+        raise ValueError(f"{what}: C's last dimension {C.shape[-1]} != {ncols} "
+                         f"({'N/2 for SiLU*mul' if epilogue == CHORD_EPI_SILU_MUL else 'N'})")
+    if C.numel() < c_rows * ncols:
+        raise ValueError(f"{what}: C holds {C.numel()} values, needs {c_rows} rows of {ncols}")
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -214,6 +235,8 @@ def chord_w4a16_moe_gemm(A, a_gather: bool, packed_w, E_local: int, N: int, K: i
                          tuning=None, dev_status=None, stream=None):
     """workspace: uint8 tensor of chord_w4a16_moe_gemm_workspace_bytes() bytes whose first
     256 bytes were zeroed once (the library keeps them zero)."""
+    cap = sorted_token_ids.numel()
+    _check_operands(A, C, K, N, epilogue, M if a_gather else cap, cap, "chord_w4a16_moe_gemm")
     tun = _tuning(tuning)
     _check(lib().chord_w4a16_moe_gemm(
         _ptr(A, None, "A"), int(a_gather), _ptr(packed_w, torch.uint8, "packed_w"), E_local, N, K, M,
@@ -233,6 +256,9 @@ def chord_w4a16_gemm_workspace_bytes(M: int) -> int:
 def chord_w4a16_gemm(A, packed_w, N: int, K: int, epilogue: int, C, workspace, tuning=None,
                      dev_status=None, stream=None):
     """Dense C = A (q*s)^T with a one-expert packed blob; workspace zeroed once when allocated."""
+    if A.dim() != 2 or C.dim() != 2 or C.shape[0] != A.shape[0]:
+        raise ValueError("chord_w4a16_gemm: A must be [M, K] and C [M, N or N/2] with the same rows")
+    _check_operands(A, C, K, N, epilogue, A.shape[0], A.shape[0], "chord_w4a16_gemm")
     tun = _tuning(tuning)
     _check(lib().chord_w4a16_gemm(
         _ptr(A, None, "A"), _ptr(packed_w, torch.uint8, "packed_w"), N, K, A.shape[0], epilogue,
@@ -249,6 +275,9 @@ def chord_w4a16_grouped_gemm_contiguous(A, group_rows, packed_w, N: int, K: int,
     """Contiguous layout: A [rows, K], expert groups in order, each padded to 128 rows."""
     if A.dim() != 2:
         raise ValueError("contiguous layout: A must be [rows, K]")
+    if C.dim() != 2 or C.shape[0] != A.shape[0]:
+        raise ValueError("contiguous layout: C must be [rows, N or N/2] with the rows of A")
+    _check_operands(A, C, K, N, epilogue, A.shape[0], A.shape[0], "chord_w4a16_grouped_gemm_contiguous")
     tun = _tuning(tuning)
     _check(lib().chord_w4a16_grouped_gemm_contiguous(
         _ptr(A, None, "A"), A.shape[0], _ptr(group_rows, torch.int32, "group_rows"), group_rows.numel(),
@@ -262,6 +291,10 @@ def chord_w4a16_grouped_gemm_masked(A, group_rows, packed_w, N: int, K: int, epi
     """Masked layout: A [E, max_m, K], the first group_rows[e] rows of expert e are used."""
     if A.dim() != 3 or group_rows.numel() != A.shape[0]:
         raise ValueError("masked layout: A must be [E, max_m, K] with one group_rows entry per expert")
+    if C.dim() != 3 or C.shape[:2] != A.shape[:2]:
+        raise ValueError("masked layout: C must be [E, max_m, N or N/2] with the experts and rows of A")
+    _check_operands(A, C, K, N, epilogue, A.shape[0] * A.shape[1], A.shape[0] * A.shape[1],
+                    "chord_w4a16_grouped_gemm_masked")
     tun = _tuning(tuning)
     _check(lib().chord_w4a16_grouped_gemm_masked(
         _ptr(A, None, "A"), _ptr(group_rows, torch.int32, "group_rows"), A.shape[0], A.shape[1], expected_m,

@@ -3,6 +3,8 @@
 // launch does everything.  More chunks: phase 1 writes chunk ranks and
 // per-chunk counts to the workspace, phase 2 adds the prefix over chunks and
 // scatters.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "align_impl.cuh"
@@ -140,8 +142,9 @@ static __device__ __align__(256) int32_t g_align_scratch[kNoAllocScratchInts];
 namespace {
 // Device address of g_align_scratch, looked up once per device.  In host code
 // the symbol name is only a host-side stand-in, so it is never passed to a
-// kernel directly.
-void* g_scratch_ptr[64] = {nullptr};
+// kernel directly.  Atomic: host threads making their first call on a device
+// at the same time may both look it up; they store the same address.
+std::atomic<void*> g_scratch_ptr[64];
 }  // namespace
 
 cudaError_t align_noalloc_scratch(void** ptr) {
@@ -149,13 +152,15 @@ cudaError_t align_noalloc_scratch(void** ptr) {
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
+  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    // With lazy module loading this lookup may be what loads the module and
+    // reserves the array on this device.
     err = cudaGetSymbolAddress(&p, g_align_scratch);
     if (err != cudaSuccess) return err;
-    g_scratch_ptr[dev] = p;
+    g_scratch_ptr[dev].store(p, std::memory_order_release);
   }
-  *ptr = g_scratch_ptr[dev];
+  *ptr = p;
   return cudaSuccess;
 }
 

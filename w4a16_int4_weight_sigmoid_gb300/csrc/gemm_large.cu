@@ -45,19 +45,36 @@ namespace chord {
 namespace {
 
 constexpr int kMRows = 128;                      // weight rows per item (2 packed tiles)
-constexpr int kMaxTok = 192;                     // tokens per pass (MMA N)
+#ifndef CHORD_LG_MAXTOK
+#define CHORD_LG_MAXTOK 192
+#endif
+#ifndef CHORD_LG_ACCBUFS
+#define CHORD_LG_ACCBUFS 2
+#endif
+#ifndef CHORD_LG_SA
+#define CHORD_LG_SA 2
+#endif
+#ifndef CHORD_LG_SB
+#define CHORD_LG_SB 3
+#endif
+#ifndef CHORD_LG_SP
+#define CHORD_LG_SP 6
+#endif
+constexpr int kMaxTok = CHORD_LG_MAXTOK;         // tokens per pass (MMA N)
+constexpr int kAccBufs = CHORD_LG_ACCBUFS;       // TMEM accumulators (2: epilogue overlaps the next item)
 constexpr int kStageUnits = 2;                   // 64-wide K units per stage
-constexpr int kSP = 6, kSB = 3, kSA = 2;         // ring depths: packed, activations, A in TMEM
+constexpr int kSP = CHORD_LG_SP, kSB = CHORD_LG_SB, kSA = CHORD_LG_SA;   // ring depths: packed, activations, A in TMEM
 constexpr int kBHalfBytes = kMaxTok * kUnitK * 2;            // 24 KB: 192 rows x 128 B
 constexpr int kBStageBytes = kStageUnits * kBHalfBytes;      // 48 KB
 constexpr int kPStageBytes = 2 * kStageUnits * kUnitBytes;   // 9216: [tile][unit]
 constexpr int kBOff = 0, kPOff = kSB * kBStageBytes;
 constexpr int kSmemBytes = kPOff + kSP * kPStageBytes + 1024;   // + alignment slack
-constexpr int kAccCols = kMaxTok;                // accumulator j at column j * 192
-constexpr int kACol0 = 2 * kAccCols;             // A slot s at column 384 + 64 s
+constexpr int kAccCols = kMaxTok;                // accumulator j at column j * kMaxTok
+constexpr int kACol0 = kAccBufs * kAccCols;      // A slot s at column kACol0 + 64 s
 constexpr int kASlotCols = kStageUnits * kUnitK / 2;         // 64
 constexpr int kTmemCols = 512;
 static_assert(kACol0 + kSA * kASlotCols <= kTmemCols, "TMEM budget");
+static_assert(kMaxTok % 64 == 0 && kMaxTok <= 256, "whole 64-row boxes never overrun an activation slot");
 constexpr int kDequantWarp0 = 4, kDequantWarps = 8;
 constexpr int kEpiWarp0 = kDequantWarp0 + kDequantWarps;   // 12: warp index % 4 = lane quarter
 constexpr int kThreads = 32 * (kEpiWarp0 + 4);
@@ -194,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t p_full[kSP], p_empty[kSP];
   __shared__ __align__(8) uint64_t b_full[kSB], b_empty[kSB];
   __shared__ __align__(8) uint64_t a_full[kSA], a_empty[kSA];
-  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], done_bar;
+  __shared__ __align__(8) uint64_t tfull_bar[kAccBufs], tempty_bar[kAccBufs], done_bar;
   __shared__ __align__(8) uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   __shared__ volatile int item_q[kItemSlots];
   __shared__ uint32_t tmem_base_s;
@@ -226,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&a_full[s], kDequantWarps);
       mbar_init(&a_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], 4);
     }
@@ -267,14 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ packed-weight producer
     if (lane == 0) {
       int it = 0;
-      bool ok = true;
       for (int q = 0;; ++q) {
         int i = atomicAdd(a.work, 1);
         if (i >= total_items || abort_flag) i = -1;
         const int slot = q % kItemSlots;
         if (q >= kItemSlots && !mbar_wait_backoff(&item_empty[slot], ((q / kItemSlots) - 1) & 1, a.status)) {
           abort_flag = 1;
-          ok = false;
           break;
         }
         item_q[slot] = i;
@@ -298,8 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_g2s(dst + kStageUnits * kUnitBytes, t0 + a.tile_bytes + src, bytes, &p_full[s]);
         }
       }
-      // the last CTA to run out of items zeroes the counters for the next launch
-      if (ok && atomicAdd(a.work + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      // the last CTA to run out of items zeroes the counters for the next
+      // launch; every CTA arrives, also one that gave up on a wait
+      if (atomicAdd(a.work + 1, 1) == static_cast<int>(gridDim.x) - 1) {
         atomicExch(a.work, 0);
         atomicExch(a.work + 1, 0);
       }
@@ -356,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
-        const int acc = j & 1, use = j >> 1;
+        const int acc = j % kAccBufs, use = j / kAccBufs;
         if (use >= 1 && !mbar_wait(&tempty_bar[acc], (use - 1) & 1, a.status)) {
           abort_flag = 1;
           break;
@@ -464,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
-      const int acc = j & 1, use = j >> 1;
+      const int acc = j % kAccBufs, use = j / kAccBufs;
       if (!mbar_wait_backoff(&tfull_bar[acc], use & 1, a.status)) {
         abort_flag = 1;
         break;

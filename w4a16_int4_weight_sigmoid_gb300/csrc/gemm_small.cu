@@ -163,7 +163,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     fence_mbar_init();
   }
   __syncthreads();
-  if (!hdr_ok) return;
+  if (!hdr_ok) {
+    // A mismatched blob computes nothing (the error is recorded above), but a
+    // programmatic launch still waits for the kernel before it and releases
+    // the next one only then, so the launch chain keeps its ordering.
+    if (a.pdl) {
+      grid_dep_wait();
+      grid_dep_launch();
+    }
+    return;
+  }
 
   const int n_units = a.K / kUnitK;
   const int k_stages = (n_units + kUnitsPerStage - 1) / kUnitsPerStage;
@@ -309,7 +318,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       }
     }
     if (lane == 0) {
-      if (ok && atomicAdd(a.work + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      // every CTA arrives, also one that gave up on a wait, so the counters
+      // are zero again after the launch whatever happened
+      if (atomicAdd(a.work + 1, 1) == static_cast<int>(gridDim.x) - 1) {
         atomicExch(a.work, 0);
         atomicExch(a.work + 1, 0);
       }
