@@ -326,7 +326,8 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
   if (!A || !packed_w || !C || !expert_counts || !expert_offsets || !expert_ids || !ntpp ||
       (a_gather && !sorted_token_ids))
     return fail(CHORD_ERR_INVALID_ARG, "null pointer");
-  if (!aligned16(A) || !aligned16(packed_w)) return fail(CHORD_ERR_INVALID_ARG, "A and packed_w must be 16-byte aligned");
+  if (!aligned16(A) || !aligned16(packed_w) || !aligned16(C))
+    return fail(CHORD_ERR_INVALID_ARG, "A, packed_w and C must be 16-byte aligned");
   if (!workspace || ws_bytes < kWorkBytes || !aligned16(workspace))
     return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "GEMM workspace must hold at least %zu aligned bytes", kWorkBytes);
   if (M == 0) return CHORD_OK;
@@ -395,7 +396,8 @@ int grouped_impl(const chord_bf16* A, size_t capacity, const int32_t* group_rows
   if (capacity > 0x7fffffffu) return fail(CHORD_ERR_INVALID_ARG, "%zu rows: too many", capacity);
   if (capacity == 0) return CHORD_OK;
   if (!A || !group_rows || !packed_w || !C) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
-  if (!aligned16(A) || !aligned16(packed_w)) return fail(CHORD_ERR_INVALID_ARG, "A and packed_w must be 16-byte aligned");
+  if (!aligned16(A) || !aligned16(packed_w) || !aligned16(C))
+    return fail(CHORD_ERR_INVALID_ARG, "A, packed_w and C must be 16-byte aligned");
   if (!workspace || !aligned16(workspace)) return fail(CHORD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   const size_t need = chord_w4a16_grouped_workspace_bytes(E, capacity);
   if (ws_bytes < need) return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "grouped GEMM workspace %zu < %zu", ws_bytes, need);

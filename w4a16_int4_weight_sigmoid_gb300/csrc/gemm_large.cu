@@ -25,12 +25,18 @@
 //     activation tiles (shared memory, 3 deep, from L2, one 2-D TMA box of
 //     up to 192 rows per 64 of K, 128-byte swizzle, by warp 2) and
 //     dequantised A tiles (TMEM, 2 deep);
-//   * warps 4-11 (dequant, one 32-row TMEM lane quarter and one 64-wide half
-//     of the stage each): INT4 -> BF16 q*s (rounded once), tcgen05.st;
+//   * warps 4-19 (dequant): two groups of eight take alternate stages (each
+//     group owns one A slot); in a group, each warp covers one 32-row TMEM
+//     lane quarter and one 64-wide half of the stage: INT4 -> BF16 q*s
+//     (rounded once), tcgen05.st.  A warp's stage is a chain of latencies
+//     (barrier waits, shared-memory loads, decode, TMEM store and fences,
+//     ~1.3k cycles measured), longer than the stage's MMAs, so one group
+//     alone left the tensor pipe idle; two groups halve the gap (prefill
+//     gate/up 593 -> 536 us on GB300);
 //   * warp 1 (MMA): TMEM allocation; the converged warp waits and one
 //     elected lane issues the MMAs (M=128) into one of two accumulators and
 //     commits slot release and item completion to mbarriers;
-//   * warps 12-15 (epilogue): tcgen05.ld of the accumulator, SiLU(gate) * up
+//   * warps 20-23 (epilogue): tcgen05.ld of the accumulator, SiLU(gate) * up
 //     (gate and up rows of one index sit 8 TMEM lanes apart) or a plain
 //     store, BF16, rows in sorted order; the second accumulator lets the next
 //     item's MMAs run meanwhile.
@@ -45,25 +51,10 @@ namespace chord {
 namespace {
 
 constexpr int kMRows = 128;                      // weight rows per item (2 packed tiles)
-#ifndef CHORD_LG_MAXTOK
-#define CHORD_LG_MAXTOK 192
-#endif
-#ifndef CHORD_LG_ACCBUFS
-#define CHORD_LG_ACCBUFS 2
-#endif
-#ifndef CHORD_LG_SA
-#define CHORD_LG_SA 2
-#endif
-#ifndef CHORD_LG_SB
-#define CHORD_LG_SB 3
-#endif
-#ifndef CHORD_LG_SP
-#define CHORD_LG_SP 6
-#endif
-constexpr int kMaxTok = CHORD_LG_MAXTOK;         // tokens per pass (MMA N)
-constexpr int kAccBufs = CHORD_LG_ACCBUFS;       // TMEM accumulators (2: epilogue overlaps the next item)
+constexpr int kMaxTok = 192;                     // tokens per pass (MMA N)
+constexpr int kAccBufs = 2;                      // TMEM accumulators: the epilogue overlaps the next item
 constexpr int kStageUnits = 2;                   // 64-wide K units per stage
-constexpr int kSP = CHORD_LG_SP, kSB = CHORD_LG_SB, kSA = CHORD_LG_SA;   // ring depths: packed, activations, A in TMEM
+constexpr int kSP = 6, kSB = 3, kSA = 2;         // ring depths: packed, activations, A in TMEM
 constexpr int kBHalfBytes = kMaxTok * kUnitK * 2;            // 24 KB: 192 rows x 128 B
 constexpr int kBStageBytes = kStageUnits * kBHalfBytes;      // 48 KB
 constexpr int kPStageBytes = 2 * kStageUnits * kUnitBytes;   // 9216: [tile][unit]
@@ -75,8 +66,14 @@ constexpr int kASlotCols = kStageUnits * kUnitK / 2;         // 64
 constexpr int kTmemCols = 512;
 static_assert(kACol0 + kSA * kASlotCols <= kTmemCols, "TMEM budget");
 static_assert(kMaxTok % 64 == 0 && kMaxTok <= 256, "whole 64-row boxes never overrun an activation slot");
-constexpr int kDequantWarp0 = 4, kDequantWarps = 8;
-constexpr int kEpiWarp0 = kDequantWarp0 + kDequantWarps;   // 12: warp index % 4 = lane quarter
+// Two groups of eight dequant warps take alternate stages.  With two A
+// slots each group owns one slot (stage it uses slot it % 2 and group
+// it % 2), so a group waits for exactly the previous phase of its own slot
+// and the parity waits cannot alias; a third group would need a third slot.
+constexpr int kGroups = 2;
+constexpr int kDequantWarp0 = 4, kGroupWarps = 8, kDequantWarps = kGroups * kGroupWarps;
+static_assert(kGroups == kSA, "each dequant group owns one A slot");
+constexpr int kEpiWarp0 = kDequantWarp0 + kDequantWarps;   // 20: warp index % 4 = lane quarter
 constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kMaxExperts = 1024;
 constexpr int kItemSlots = 4;
@@ -233,14 +230,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_flag = 0;
     for (int s = 0; s < kSP; ++s) {
       mbar_init(&p_full[s], 1);
-      mbar_init(&p_empty[s], kDequantWarps);
+      mbar_init(&p_empty[s], kGroupWarps);
     }
     for (int s = 0; s < kSB; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
     }
     for (int s = 0; s < kSA; ++s) {
-      mbar_init(&a_full[s], kDequantWarps);
+      mbar_init(&a_full[s], kGroupWarps);
       mbar_init(&a_empty[s], 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
@@ -421,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // This warp: TMEM lane quarter q (rows 32q..32q+31 = slabs 2q, 2q+1 of
     // the 128-row item) and unit hu (K 64*hu .. 64*hu+63) of each stage.
     const int dq = warp - kDequantWarp0;
-    const int q = warp & 3, hu = dq >> 2;
+    const int grp = dq / kGroupWarps;
+    const int q = warp & 3, hu = (dq % kGroupWarps) >> 2;
     const int g = lane >> 2;
     const uint32_t mask = a.nib_mask, magic = a.nib_magic;   // run-time: kept in registers
     // packed offsets of slab sl (0, 1) within a stage: tile, unit, slab-in-tile
@@ -443,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       for (int ks = 0; ks < n_stages; ++ks, ++it) {
+        if ((it % kGroups) != grp) continue;
         const int sp = it % kSP, sa = it % kSA;
         bool ok = mbar_wait(&p_full[sp], (it / kSP) & 1, a.status) &&
                   (it < kSA || mbar_wait(&a_empty[sa], ((it / kSA) - 1) & 1, a.status));
