@@ -225,17 +225,26 @@ int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E,
  *            re-check every row index against these buffers.
  *   C        BF16 [capacity, N] (STORE) or [capacity, N/2] (SILU_MUL); padding
  *            rows are not written
- *   workspace  chord_w4a16_moe_gemm_workspace_bytes() bytes, 16-byte aligned.
- *            Its first 256 bytes are work-queue counters: zero them once when
- *            the workspace is allocated; every call leaves them zero (the
- *            last CTA of each launch resets them, also after a device
- *            timeout).  With a_gather = 1 the
- *            tensor-core path also stages the gathered rows there.
+ *   workspace  chord_w4a16_moe_gemm_workspace_bytes() bytes, 16-byte aligned;
+ *            zero it once when it is allocated.  Layout: 256 bytes of
+ *            work-queue counters, then the split-K area (arrival counters
+ *            and partial accumulators, about 4 MB), then, with a_gather = 1
+ *            on the tensor-core path, the gathered rows.  Every call leaves
+ *            the counters zero (the last CTA of a launch resets the queue,
+ *            also after a device timeout; the last split of an item resets
+ *            its counter).
  *   dev_status  device int for errors found on the device (may be NULL)
  * Two paths ([Humming] "워크로드별 튜닝 및 JIT 컴파일": async-copy + MMA at
  * small batch, TMA + UMMA at large batch), chosen from the expected rows per
  * expert M*topk/E_local unless tuning->path says otherwise: a weight-
  * streaming register-MMA path, and a tcgen05/TMEM path (needs N % 128 == 0).
+ * Split-K, gated on grid saturation ([Chord] "인덱스 커널 기법": stream-K
+ * only where the grid is not already full): on the register-MMA path, when
+ * the launch has at most half as many work items (64 weight rows x one
+ * BLOCK_M block) as resident CTAs and block_m <= the rows per pass, the
+ * kernel splits K into up to 8 ranges of 512 and the last range of each
+ * item to finish adds the FP32 partials in range order, so results are
+ * deterministic; it is decided on the device from num_tokens_post_padded.
  * Everything is read on the device, so the call never waits for the host.
  */
 size_t chord_w4a16_moe_gemm_workspace_bytes(size_t capacity, int K, int a_gather);
@@ -254,9 +263,9 @@ int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w
  *   A          BF16 [M, K] (16-byte aligned)
  *   C          BF16 [M, N] (STORE) or [M, N/2] (SILU_MUL)
  *   workspace  chord_w4a16_gemm_workspace_bytes(M) bytes, 16-byte aligned;
- *              zero it once when allocated (its first 256 bytes are
- *              work-queue counters that every call leaves zero); each call
- *              writes the one-expert block map into the rest on the device
+ *              zero it once when allocated (its work-queue and split-K
+ *              counters are left zero by every call); each call writes the
+ *              one-expert block map into it on the device
  * Path and rows per pass as chord_w4a16_moe_gemm with M rows per expert,
  * unless tuning says otherwise.  Errors as chord_w4a16_moe_gemm.
  */
@@ -286,8 +295,8 @@ int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, in
  *   C            BF16, the same row layout as A, N (STORE) or N/2 columns;
  *                rows past an expert's group_rows are not written
  *   workspace    chord_w4a16_grouped_workspace_bytes(E, rows of A) bytes,
- *                16-byte aligned, its first 256 bytes zeroed once when
- *                allocated (kept zero by every call)
+ *                16-byte aligned, zeroed once when allocated (its counters
+ *                are left zero by every call)
  * Host-side errors return CHORD_ERR_* and launch nothing; a count outside
  * [0, max_m] (masked) or a padded total above the rows of A (contiguous) is
  * recorded in *dev_status as CHORD_ERR_INVALID_ARG and nothing is computed.
@@ -322,7 +331,10 @@ int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t*
  *   out          BF16 [M, H]
  *   topk_weights_out FP32 [M, topk], topk_ids_out INT32 [M, topk]: optional
  *                copies of the routing (may be NULL)
- *   workspace    chord_moe_layer_workspace_bytes() bytes
+ *   workspace    chord_moe_layer_workspace_bytes() bytes, 16-byte aligned,
+ *                any contents (every call zeroes its own counters with one
+ *                memset); it holds the routing, the align buffers, h, y,
+ *                and the GEMMs' work-queue and split-K state
  * The expert-parallel shard is implied by E_local < E_total ([Chord]
  * "런타임 고려사항": the profile is inferred from the shapes, no shard
  * argument).  Weights are normalised over all topk experts, local or not.
@@ -337,8 +349,8 @@ size_t chord_moe_layer_workspace_bytes(int M, int H, int I, int E_local, int top
 /* Host-only: the tuning chord_moe_layer uses for these shapes (tokens-per-
  * expert policy, [Chord] "인덱스 커널 기법": the schedule follows the tokens
  * delivered per expert, tok_e = M*topk/E_total; the tcgen05 path from
- * tok_e >= 10, where the two paths measured even on GB300, the register-MMA
- * path below it with 8 or 16 rows per pass).  Writes *plan; returns
+ * tok_e >= 12, where the two paths measured even on GB300, the register-MMA
+ * path below it with 8, 16 or 32 rows per pass).  Writes *plan; returns
  * CHORD_OK or CHORD_ERR_INVALID_ARG.  Passing the plan to
  * chord_w4a16_moe_gemm reproduces the layer's launches exactly. */
 int chord_moe_layer_plan(int M, int E_total, int topk, chord_tuning* plan);

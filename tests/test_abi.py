@@ -66,8 +66,11 @@ def test_sizing_functions(L):
     assert plan.path == chord.CHORD_PATH_SMALL_M and plan.rows_per_pass == 8
     assert chord.chord_moe_layer_plan(8192, 384, 8).path == chord.CHORD_PATH_LARGE_M
     assert chord.chord_moe_layer_plan(128, 4, 2).rows_per_pass == 32
-    assert L.chord_w4a16_moe_gemm_workspace_bytes(1000, 512, 0) == 256
-    assert L.chord_w4a16_moe_gemm_workspace_bytes(1000, 512, 1) == 256 + 1000 * 512 * 2
+    # 256 B of work-queue counters, the split-K area (512 items x 4 warps of
+    # counters, 512 slots of 8 KB partials), then the gathered rows
+    split = 512 * 4 * 4 + 512 * 2048 * 4
+    assert L.chord_w4a16_moe_gemm_workspace_bytes(1000, 512, 0) == 256 + split
+    assert L.chord_w4a16_moe_gemm_workspace_bytes(1000, 512, 1) == 256 + split + 1000 * 512 * 2
 
 
 def _rc_and_msg(L, rc):
@@ -96,27 +99,27 @@ def test_argument_checks_reject_before_launch(L):
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # gate_up needs N % 64
     t = chord.chord_tuning(0, 0, 1, 0)
     rc, msg = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 0,
-                                                    P, ctypes.byref(t), P, 1 << 20, None, None))
+                                                    P, ctypes.byref(t), P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_UNSUPPORTED and "FP16" in msg
     t = chord.chord_tuning(0, 0, 0, 1)
     rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 0,
-                                                  P, ctypes.byref(t), P, 1 << 20, None, None))
+                                                  P, ctypes.byref(t), P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_UNSUPPORTED
     rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 100, 8, 2, P, P, P, P, P, 16, 100, 0,
-                                                  P, None, P, 1 << 20, None, None))
+                                                  P, None, P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # K % 64
     rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 96, 128, 8, 2, P, P, P, P, P, 16, 100, 1,
-                                                  P, None, P, 1 << 20, None, None))
+                                                  P, None, P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # SiLU needs N % 64
     rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 12, 100, 0,
-                                                  P, None, P, 1 << 20, None, None))
+                                                  P, None, P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # block_m
     rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 0,
                                                   P, None, P, 100, None, None))
-    assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL                # < 256 B of counters
+    assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL                # < counters + split-K area
     t = chord.chord_tuning(chord.CHORD_PATH_LARGE_M, 0, 0, 0)
     rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 192, 128, 8, 2, P, P, P, P, P, 16, 100, 0,
-                                                  P, ctypes.byref(t), P, 1 << 20, None, None))
+                                                  P, ctypes.byref(t), P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_UNSUPPORTED                        # tcgen05 path needs N % 128
     rc, _ = _rc_and_msg(L, L.chord_moe_sum(P, P, P, 4, 2, 100, P, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # H % 8
@@ -145,9 +148,9 @@ def test_new_entry_points_reject_before_launch(L):
                                                      None, None, 0, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG and "capacity" in msg
     # dense GEMM: K % 64, SiLU needs N % 64, workspace too small, tcgen05 path needs N % 128
-    rc, _ = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 256, 100, 8, 0, P, None, P, 1 << 20, None, None))
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 256, 100, 8, 0, P, None, P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG
-    rc, _ = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 96, 128, 8, 1, P, None, P, 1 << 20, None, None))
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 96, 128, 8, 1, P, None, P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG
     need = L.chord_w4a16_gemm_workspace_bytes(1000)
     assert need >= 512 + (1000 // 8) * 4

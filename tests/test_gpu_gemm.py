@@ -181,3 +181,36 @@ def test_dense_gemm(M, K, N, epi, path):
         assert int(ws[:256].view(torch.int32).abs().sum().item()) == 0
         tol = GEMM_TOL[LARGE] if path == LARGE or (path == 0 and M >= 64 and N % 128 == 0) else GEMM_TOL[SMALL]
         assert_close_to_oracle(bf16_to_np(C), ref, "dense", *tol)
+
+
+def test_gemm_split_k_counters_and_parity():
+    """Three tokens, K = 2048 (four 512-wide stages), 8 experts: 8 or fewer
+    work items against hundreds of resident CTAs, so the decode GEMM splits
+    K.  The split partials are written (the area is no longer zero), the
+    per-item counters are back at zero after the call, every row matches the
+    oracle, and a second call gives the same bits."""
+    M, K, N, E, topk, bm = 3, 2048, 256, 8, 2, 8
+    ids, al, x, q, s = _problem(M, K, N, E, E, 0, topk, 41, bm)
+    up = _upload_align(al, M, topk, E, bm)
+    cap = up[0]
+    packed = prepack(to_device(q), to_device(s), False)
+    ws = torch.zeros(chord.chord_w4a16_moe_gemm_workspace_bytes(cap, K, True), dtype=torch.uint8, device="cuda")
+    tun = chord.chord_tuning(SMALL, 0, 0, 0)
+    outs = []
+    for _ in range(2):
+        C = torch.full((cap, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        chord.chord_w4a16_moe_gemm(to_device(x), True, packed, E, N, K, M, topk, *up[1:], bm, STORE, C, ws,
+                                   tuning=tun, dev_status=status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        counters = ws[256:256 + 512 * 4 * 4].view(torch.int32)
+        assert int(counters.abs().sum().item()) == 0, "split-K counters must be left at zero"
+        assert int(ws[:256].view(torch.int32).abs().sum().item()) == 0
+        partials = ws[256 + 512 * 16:256 + 512 * 16 + 512 * 2048 * 4]
+        assert int((partials != 0).sum().item()) > 0, "no split-K partials were written"
+        outs.append(bf16_to_np(C))
+        for e, (rows, ref) in _oracle_rows(x, q, s, al, topk, STORE, True).items():
+            assert_close_to_oracle(outs[-1][rows], ref, f"split-K expert {e}", *GEMM_TOL[SMALL])
+    n = al["num_tokens_post_padded"]
+    assert np.array_equal(outs[0][:n].view(np.uint16), outs[1][:n].view(np.uint16))

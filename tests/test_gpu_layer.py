@@ -108,8 +108,61 @@ def test_layer_kimi_workloads_sampled(shape):
     rng = np.random.default_rng(shape.seed)
     local = np.any((ids >= shape.expert_begin) & (ids < shape.expert_begin + shape.E_local), axis=1)
     cand = np.nonzero(local)[0]
-    tokens = np.sort(rng.choice(cand, size=min(6, cand.size), replace=False))
+    # every touched local expert contributes the tokens of its first and last
+    # assignment (its first and last sorted rows, so the first and the last
+    # pass of an expert whose rows take several passes), plus a seeded sample
+    flat = ids.ravel()
+    chosen = set(rng.choice(cand, size=min(6, cand.size), replace=False).tolist())
+    for e in range(shape.expert_begin, shape.expert_begin + shape.E_local):
+        f = np.nonzero(flat == e)[0]
+        if f.size:
+            chosen.update((int(f[0]) // shape.topk, int(f[-1]) // shape.topk))
+    tokens = np.array(sorted(chosen), dtype=np.int64)
     ref = oracle.moe_layer_tokens(tokens, d["x"], d["logits"], d["bias"], d["w13_q"], d["w13_s"],
                                   d["w2_q"], d["w2_s"], shape.topk, shape.expert_begin)
     assert_close_to_oracle(got[tokens], ref, shape.name)
     assert np.all(np.isfinite(got))
+
+
+# Few tokens with K of several 512-wide stages: the decode GEMM sees far fewer
+# work items than resident CTAs and splits K (split-K gated on the grid);
+# every output element against the oracle, and repeated calls bit-identical
+# (the split partials are added in split order whatever CTA finishes last).
+SPLIT_K = [
+    small("split_k_two_tokens", 2, 2048, 512, 32, 8, 0, 4, 27),
+    small("split_k_one_token_both_gemms", 1, 1024, 1024, 8, 4, 0, 2, 28),
+    small("split_k_ragged_shard", 3, 1536, 768, 24, 6, 3, 5, 29),
+]
+
+
+@pytest.mark.parametrize("shape", SPLIT_K, ids=lambda s: s.name)
+def test_layer_split_k_full_parity(shape):
+    d = wl.layer_inputs(shape)
+    ref, w, ids = oracle.moe_layer(d["x"], d["logits"], d["bias"], d["w13_q"], d["w13_s"],
+                                   d["w2_q"], d["w2_s"], shape.topk, shape.expert_begin)
+    first = None
+    for _ in range(3):
+        _, got, gw, gids = run_layer(shape, d)
+        assert np.array_equal(gids, ids)
+        assert_close_to_oracle(got, ref, shape.name)
+        if first is None:
+            first = got
+        else:
+            assert np.array_equal(got, first), "split-K result changed between calls"
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_layer_kimi_ep8_few_tokens(M):
+    """Kimi-K2 EP8 shapes at 1 and 4 tokens: the split-K decode path on both
+    GEMMs (64 and 112 weight tiles against 608 resident CTAs), every token
+    against the oracle."""
+    base = wl.EP8_DECODE
+    shape = wl.LayerShape(f"kimi_ep8_m{M}", M, base.H, base.I, base.E_total, base.E_local, 0,
+                          base.topk, 31 + M)
+    d = wl.layer_inputs(shape)
+    _, got, gw, gids = run_layer(shape, d)
+    w, ids, _ = oracle.route(d["logits"], d["bias"], shape.topk)
+    assert np.array_equal(gids, ids)
+    ref = oracle.moe_layer_tokens(np.arange(M), d["x"], d["logits"], d["bias"], d["w13_q"], d["w13_s"],
+                                  d["w2_q"], d["w2_s"], shape.topk, shape.expert_begin)
+    assert_close_to_oracle(got, ref, shape.name)

@@ -58,11 +58,33 @@ int rows_per_pass_for(double tok_e) {
 constexpr double kLargeTokE = 64.0;
 // chord_moe_layer's policy: expected rows per expert M*topk/E_total at or
 // above which the tcgen05 path is used.  Measured on GB300 at Kimi EP8
-// shapes (whole layer, both paths forced): M = 256 -> register path 288 us
-// vs 397 us; M = 512 -> 439 vs 434 us; M = 1024 -> 936 vs 464 us, so the
-// paths cross at about 10 rows per expert.
-constexpr double kLayerLargeTokE = 10.0;
+// shapes (whole layer, both paths forced, split-K decode GEMM and two
+// dequant groups on the tcgen05 path): M = 256 -> register path 231 us vs
+// 333 us; M = 512 -> 317 vs 366 us; M = 1024 -> 655 vs 398 us, so the
+// paths cross near M = 590, 12 rows per expert.
+constexpr double kLayerLargeTokE = 12.0;
 constexpr size_t kWorkBytes = 256;   // work-queue counters at the start of a GEMM workspace
+// split-K area of a GEMM workspace: arrival counters, then partial accumulators
+constexpr size_t kSplitCnt = chord::kSplitCntBytes;
+constexpr size_t kSplitBytes = chord::kSplitCntBytes + chord::kSplitPartialBytes;
+
+// Where one GEMM launch keeps its state on the device.
+struct GemmWs {
+  int* work = nullptr;              // 2 work-queue counters, zero between launches
+  int* split_cnt = nullptr;         // split-K counters, zero between launches (NULL: no split-K)
+  float* split_partial = nullptr;   // split-K partial accumulators
+  uint16_t* gather = nullptr;       // tcgen05 path with gathered rows: [capacity, K] BF16
+  size_t gather_bytes = 0;
+};
+
+// [work counters | split counters | split partials] at the start of p.
+GemmWs carve_gemm_ws(char* p) {
+  GemmWs w;
+  w.work = reinterpret_cast<int*>(p);
+  w.split_cnt = reinterpret_cast<int*>(p + kWorkBytes);
+  w.split_partial = reinterpret_cast<float*>(p + kWorkBytes + kSplitCnt);
+  return w;
+}
 
 // BLOCK_M the layer aligns with: one small-M pass per block, or 16 (the
 // tcgen05 path pads each expert's rows to 16 only).
@@ -71,7 +93,7 @@ int layer_block_m(const chord_tuning& plan) {
 }
 
 struct LayerWs {
-  size_t work, tw, ids, sorted, eids, ntpp, counts, offsets, pos, align_ws, h, y, total;
+  size_t work, partial, tw, ids, sorted, eids, ntpp, counts, offsets, pos, align_ws, h, y, total;
   size_t cap;
   int bm;
 };
@@ -97,10 +119,13 @@ LayerWs layer_ws(int M, int H, int I, int E_local, int topk, int bm) {
   w.pos = take(mk * sizeof(int32_t));
   w.align_ws = take(chord::align_workspace_bytes(static_cast<long long>(mk), E_local));
   w.h = take(w.cap * static_cast<size_t>(I) * 2);
-  // [down GEMM counters | gate/up GEMM counters | y]: the gate/up workspace is
-  // its counters followed by y's region, which holds the gathered x rows of
-  // the tcgen05 path until the down GEMM writes y.
-  w.work = take(2 * kWorkBytes);
+  // Counters, zeroed by one memset per call: [down work | gate/up work |
+  // down split-K | gate/up split-K]; then the split-K partials, shared by
+  // the two GEMMs (the down GEMM writes them only after the gate/up GEMM
+  // has completed); then y, whose region holds the gathered x rows of the
+  // tcgen05 gate/up path until the down GEMM writes y.
+  w.work = take(2 * kWorkBytes + 2 * kSplitCnt);
+  w.partial = take(chord::kSplitPartialBytes);
   w.y = take(w.cap * static_cast<size_t>(H) * 2);
   w.total = o;
   return w;
@@ -315,8 +340,8 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
                      int K, int M, int topk, const int32_t* sorted_token_ids,
                      const int32_t* expert_ids, const int32_t* ntpp, const int32_t* expert_counts,
                      const int32_t* expert_offsets, int block_m, size_t capacity, int epilogue,
-                     chord_bf16* C, const chord_tuning* tuning, double tok_e, void* workspace,
-                     size_t ws_bytes, int* dev_status, void* stream, int pdl = 0) {
+                     chord_bf16* C, const chord_tuning* tuning, double tok_e, const GemmWs& ws,
+                     int* dev_status, void* stream, int pdl = 0) {
   int rc = check_tuning(tuning);
   if (rc) return rc;
   rc = check_gemm_shapes(N, K, epilogue);
@@ -328,8 +353,7 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
     return fail(CHORD_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(A) || !aligned16(packed_w) || !aligned16(C))
     return fail(CHORD_ERR_INVALID_ARG, "A, packed_w and C must be 16-byte aligned");
-  if (!workspace || ws_bytes < kWorkBytes || !aligned16(workspace))
-    return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "GEMM workspace must hold at least %zu aligned bytes", kWorkBytes);
+  if (!ws.work) return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "no GEMM workspace");
   if (M == 0) return CHORD_OK;
   int path = tuning && tuning->path ? tuning->path : CHORD_PATH_AUTO;
   if (path == CHORD_PATH_AUTO)
@@ -351,7 +375,9 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
   g.counts = expert_counts;
   g.offsets = expert_offsets;
   g.block_m = block_m;
-  g.work = static_cast<int*>(workspace);
+  g.work = ws.work;
+  g.split_cnt = ws.split_cnt;
+  g.split_partial = ws.split_partial;
   g.epilogue = epilogue;
   g.C = C;
   g.status = dev_status;
@@ -363,10 +389,10 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
   if (path == CHORD_PATH_LARGE_M) {
     const uint16_t* B = A;
     if (a_gather) {
-      const size_t need = kWorkBytes + capacity * static_cast<size_t>(K) * 2;
-      if (ws_bytes < need)
-        return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "GEMM workspace %zu < required %zu", ws_bytes, need);
-      uint16_t* xs = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + kWorkBytes);
+      const size_t need = capacity * static_cast<size_t>(K) * 2;
+      if (!ws.gather || ws.gather_bytes < need)
+        return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "GEMM workspace: gathered rows need %zu bytes", need);
+      uint16_t* xs = ws.gather;
       e = chord::gather_rows_launch(A, sorted_token_ids, ntpp, topk, M * topk, K, capacity, xs, st);
       if (e != cudaSuccess) return cuda_fail(e, "gather launch");
       B = xs;
@@ -416,22 +442,26 @@ int grouped_impl(const chord_bf16* A, size_t capacity, const int32_t* group_rows
   int32_t* meta = reinterpret_cast<int32_t*>(ws + kWorkBytes);
   int32_t *counts = meta, *offsets = meta + E, *ntpp = meta + 2 * E + 1;
   int32_t* eids = reinterpret_cast<int32_t*>(ws + kWorkBytes + round_up((2 * static_cast<size_t>(E) + 2) * 4, 256));
+  GemmWs gws = carve_gemm_ws(ws + need - kSplitBytes - kWorkBytes);
+  gws.work = reinterpret_cast<int*>(ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = chord::grouped_setup_launch(group_rows, E, masked, max_m, bm, static_cast<long long>(capacity),
                                               counts, offsets, ntpp, eids, dev_status, st);
   if (e != cudaSuccess) return cuda_fail(e, "grouped setup launch");
   return gemm_impl(A, 0, packed_w, E, N, K, static_cast<int>(capacity), 1, nullptr, eids, ntpp, counts, offsets, bm,
-                   capacity, epilogue, C, &plan, tok_e, ws, kWorkBytes, dev_status, stream);
+                   capacity, epilogue, C, &plan, tok_e, gws, dev_status, stream);
 }
 
 }  // namespace
 
 extern "C" {
 
-// [256 B work counters | counts, offsets, ntpp | expert_ids for up to rows/8 blocks]
+// [256 B work counters | counts, offsets, ntpp | expert_ids for up to rows/8
+// blocks | split-K counters | split-K partials]
 size_t chord_w4a16_grouped_workspace_bytes(int E, size_t rows) {
   if (E < 1 || E > 1024) return 0;
-  return kWorkBytes + round_up((2 * static_cast<size_t>(E) + 2) * 4, 256) + round_up((rows / 8 + 1) * 4, 256);
+  return kWorkBytes + round_up((2 * static_cast<size_t>(E) + 2) * 4, 256) + round_up((rows / 8 + 1) * 4, 256) +
+         kSplitBytes;
 }
 
 int chord_w4a16_grouped_gemm_contiguous(const chord_bf16* A, size_t a_rows, const int32_t* group_rows, int E,
@@ -454,8 +484,9 @@ int chord_w4a16_grouped_gemm_masked(const chord_bf16* A, const int32_t* group_ro
                       epilogue, C, tuning, workspace, ws_bytes, dev_status, stream);
 }
 
+// [256 B work counters | split-K counters | split-K partials | gathered rows]
 size_t chord_w4a16_moe_gemm_workspace_bytes(size_t capacity, int K, int a_gather) {
-  return kWorkBytes + (a_gather ? capacity * static_cast<size_t>(K > 0 ? K : 0) * 2 : 0);
+  return kWorkBytes + kSplitBytes + (a_gather ? capacity * static_cast<size_t>(K > 0 ? K : 0) * 2 : 0);
 }
 
 int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w, int E_local,
@@ -465,15 +496,26 @@ int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w
                          size_t capacity, int epilogue, chord_bf16* C, const chord_tuning* tuning,
                          void* workspace, size_t ws_bytes, int* dev_status, void* stream) {
   const double tok_e = E_local > 0 ? static_cast<double>(M) * topk / E_local : 0.0;
+  int rc = check_tuning(tuning);   // argument errors take precedence over the workspace size
+  if (rc) return rc;
+  rc = check_gemm_shapes(N, K, epilogue);
+  if (rc) return rc;
+  if (!workspace || !aligned16(workspace) || ws_bytes < kWorkBytes + kSplitBytes)
+    return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "GEMM workspace must hold at least %zu aligned bytes",
+                kWorkBytes + kSplitBytes);
+  GemmWs gws = carve_gemm_ws(static_cast<char*>(workspace));
+  gws.gather = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + kWorkBytes + kSplitBytes);
+  gws.gather_bytes = ws_bytes - kWorkBytes - kSplitBytes;
   return gemm_impl(A, a_gather, packed_w, E_local, N, K, M, topk, sorted_token_ids, expert_ids,
                    num_tokens_post_padded, expert_counts, expert_offsets, block_m, capacity, epilogue,
-                   C, tuning, tok_e, workspace, ws_bytes, dev_status, stream);
+                   C, tuning, tok_e, gws, dev_status, stream);
 }
 
-// [256 B work counters | counts, offsets, ntpp (256 B) | expert_ids]
+// [256 B work counters | counts, offsets, ntpp (256 B) | expert_ids |
+// split-K counters | split-K partials]
 size_t chord_w4a16_gemm_workspace_bytes(int M) {
   if (M < 0) return 0;
-  return 2 * kWorkBytes + round_up((static_cast<size_t>(M) / 8 + 1) * sizeof(int32_t), 256);
+  return 2 * kWorkBytes + round_up((static_cast<size_t>(M) / 8 + 1) * sizeof(int32_t), 256) + kSplitBytes;
 }
 
 int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, int M, int epilogue,
@@ -503,12 +545,14 @@ int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, in
   int32_t* meta = reinterpret_cast<int32_t*>(ws + kWorkBytes);
   int32_t *counts = meta, *offsets = meta + 4, *ntpp = meta + 8;
   int32_t* eids = reinterpret_cast<int32_t*>(ws + 2 * kWorkBytes);
+  GemmWs gws = carve_gemm_ws(ws + need - kSplitBytes - kWorkBytes);
+  gws.work = reinterpret_cast<int*>(ws);
   cudaError_t e = chord::dense_setup_launch(M, bm, counts, offsets, ntpp, eids, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "dense setup launch");
   // direct rows: A is [M, K]; the tensor-core path's activation map covers
   // exactly those M rows (reads past them return zeros)
   return gemm_impl(A, 0, packed_w, 1, N, K, M, 1, nullptr, eids, ntpp, counts, offsets, bm,
-                   static_cast<size_t>(M), epilogue, C, &plan, tok_e, ws, kWorkBytes, dev_status, stream);
+                   static_cast<size_t>(M), epilogue, C, &plan, tok_e, gws, dev_status, stream);
 }
 
 }  // extern "C"
@@ -594,7 +638,7 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
   chord_bf16* y = reinterpret_cast<chord_bf16*>(ws + w.y);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  cudaError_t ce = cudaMemsetAsync(ws + w.work, 0, 2 * kWorkBytes, st);
+  cudaError_t ce = cudaMemsetAsync(ws + w.work, 0, 2 * kWorkBytes + 2 * kSplitCnt, st);
   if (ce != cudaSuccess) return cuda_fail(ce, "work counter reset");
   // Register-MMA path: every kernel after the router is a programmatic
   // launch, so its launch and prologue overlap the end of the kernel before
@@ -607,12 +651,19 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
                         stream, pdl);
   if (rc) return rc;
   const double tok_e = static_cast<double>(M) * topk / E_total;
+  GemmWs ws_gu, ws_dn;
+  ws_dn.work = reinterpret_cast<int*>(ws + w.work);
+  ws_gu.work = reinterpret_cast<int*>(ws + w.work + kWorkBytes);
+  ws_dn.split_cnt = reinterpret_cast<int*>(ws + w.work + 2 * kWorkBytes);
+  ws_gu.split_cnt = reinterpret_cast<int*>(ws + w.work + 2 * kWorkBytes + kSplitCnt);
+  ws_dn.split_partial = ws_gu.split_partial = reinterpret_cast<float*>(ws + w.partial);
+  ws_gu.gather = y;   // the gathered x rows live in y's region until the down GEMM writes y
+  ws_gu.gather_bytes = w.cap * static_cast<size_t>(H) * 2;
   rc = gemm_impl(x, 1, w13_packed, E_local, 2 * I, H, M, topk, sorted, eids, ntpp, counts, offsets,
-                 w.bm, w.cap, CHORD_EPI_SILU_MUL, h, &plan, tok_e, ws + w.work + kWorkBytes,
-                 kWorkBytes + w.cap * static_cast<size_t>(H) * 2, dev_status, stream, pdl ? 1 : 0);
+                 w.bm, w.cap, CHORD_EPI_SILU_MUL, h, &plan, tok_e, ws_gu, dev_status, stream, pdl ? 1 : 0);
   if (rc) return rc;
   rc = gemm_impl(h, 0, w2_packed, E_local, H, I, M, topk, sorted, eids, ntpp, counts, offsets, w.bm,
-                 w.cap, CHORD_EPI_STORE, y, &plan, tok_e, ws + w.work, kWorkBytes, dev_status, stream,
+                 w.cap, CHORD_EPI_STORE, y, &plan, tok_e, ws_dn, dev_status, stream,
                  pdl ? 2 : 0);
   if (rc) return rc;
   return moe_sum_impl(y, tw, pos, M, topk, H, out, stream, pdl, static_cast<int>(w.cap));

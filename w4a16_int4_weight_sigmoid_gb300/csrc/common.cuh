@@ -80,6 +80,24 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   return v;
 }
 
+// Four FP32 values, cached in L2 only: for data another CTA wrote (after a
+// fence and an atomic that orders it), which this SM's L1 may hold stale.
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Split-K workspace of the decode GEMM: kSplitSlots slots of partial
+// accumulators (4 consumer warps x 32 lanes x 4 x up to 4 token tiles, FP32)
+// and one arrival counter per (item, consumer warp).
+constexpr int kSplitSlots = 512;
+constexpr int kSplitSlotFloats = 4 * 32 * 4 * 4;
+constexpr size_t kSplitCntBytes = static_cast<size_t>(kSplitSlots) * 4 * sizeof(int);
+constexpr size_t kSplitPartialBytes = static_cast<size_t>(kSplitSlots) * kSplitSlotFloats * sizeof(float);
+
 // Launch a kernel, with programmatic stream serialization when pdl is set.
 template <typename... P, typename... A>
 inline cudaError_t launch_kernel(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

@@ -33,7 +33,17 @@
 //     5-12 % slower;
 //   * epilogue: SiLU(gate) * up (a gate/up slab holds gate rows g and up rows
 //     g + 8 of the same intermediate index, so both land in one thread) or a
-//     plain store, BF16, rows in sorted order.
+//     plain store, BF16, rows in sorted order;
+//   * split-K, gated on grid saturation ([Chord] "인덱스 커널 기법": stream-K
+//     only where the grid is not already full): when a launch has at most
+//     half as many items as resident CTAs (a few decode tokens touching one
+//     or two experts), every item is split into S <= 8 ranges of K stages so
+//     that all CTAs stream weights.  Each split writes its FP32 partial
+//     accumulators to the workspace; the last split of an item to arrive
+//     (per-item counters, reset by that last arrival) adds the S partials in
+//     split order, so the result does not depend on which CTA finishes last,
+//     and runs the epilogue.  The decision is taken on the device from the
+//     block count, so it needs no host synchronisation.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -55,6 +65,15 @@ struct SmallCfg {
 };
 
 constexpr int kItemSlots = 4;
+constexpr int kMaxSplit = 8;
+
+// A work item as the producer hands it to the consumers.  rows = -1: end.
+struct SItem {
+  int tile, e, row0, rows;   // 64-row weight tile, local expert, first sorted row, rows of the block
+  int ks0, ks1;              // K stages [ks0, ks1) of this split
+  int base;                  // item index without the split (counter index)
+  int split;                 // split index | (number of splits << 16)
+};
 
 struct SmallArgs {
   const uint16_t* A;
@@ -70,6 +89,8 @@ struct SmallArgs {
   int* status;
   int N, K, topk, ldc, n_tiles, E_local;
   int pdl, max_blocks;   // programmatic-launch mode (GemmLaunch::pdl); capacity / block_m
+  float* partial;        // split-K partial accumulators (kSplitSlots slots); NULL: no split-K
+  int* split_cnt;        // per (item, consumer warp) arrival counters, zero between launches
   int64_t tile_bytes;
   uint32_t need_flags;
   // decode constants, passed at run time so they stay in registers
@@ -145,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
   __shared__ __align__(8) uint64_t item_full[kItemSlots];
   __shared__ __align__(8) uint64_t item_empty[kItemSlots];
-  __shared__ int4 item_q[kItemSlots];   // {tile, expert, first sorted row, rows} or rows = -1: end
+  __shared__ SItem item_q[kItemSlots];
   __shared__ int hdr_ok;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -200,25 +221,29 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       return how == 0 ? __ldg(p) : how == 1 ? ld_ca(p) : ld_cg(p);
     };
     const int how = a.pdl ? 1 : 0;   // after the wait
-    auto decode_item = [&](int i, long long total, int nblocks, int how) {
-      int4 item = make_int4(0, 0, 0, -1);
+    // item i -> split s of base item i / S = (tile, block), block index fastest
+    auto decode_item = [&](int i, long long total, int nblocks, int nsplit, int how) {
+      SItem item{0, 0, 0, -1, 0, 0, 0, 0};
       if (i < total) {
-        const int nt = i / nblocks, b = i - nt * nblocks;
+        const int base = i / nsplit, sp = i - base * nsplit;
+        const int nt = base / nblocks, b = base - nt * nblocks;
         const int e = ld_map(a.expert_ids + b, how);
-        item = make_int4(nt, 0, 0, 0);
+        item = SItem{nt, 0, 0, 0, sp * k_stages / nsplit, (sp + 1) * k_stages / nsplit, base, sp | (nsplit << 16)};
         if (e >= 0 && e < a.E_local) {
           const int row0 = b * a.block_m;
           const int end = ld_map(a.offsets + e, how) + ld_map(a.counts + e, how);
-          item = make_int4(nt, e, row0, max(min(a.block_m, end - row0), 0));
+          item.e = e;
+          item.row0 = row0;
+          item.rows = max(min(a.block_m, end - row0), 0);
         } else {
           set_status(a.status, CHORD_ERR_ROUTING_INVALID);
         }
       }
       return item;
     };
-    auto weight_tile = [&](const int4& item) {
+    auto weight_tile = [&](const SItem& item) {
       return a.packed + kPackHeaderBytes +
-             (static_cast<size_t>(item.y) * a.n_tiles + item.x) * static_cast<size_t>(a.tile_bytes);
+             (static_cast<size_t>(item.e) * a.n_tiles + item.tile) * static_cast<size_t>(a.tile_bytes);
     };
     // weights of stage ks into ring slot s, the slot expecting `rows` rows too
     auto issue_weights = [&](const uint8_t* wtile, int rows, int ks, int s) {
@@ -231,19 +256,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       __syncwarp();
     };
     // activation rows of stage ks of one pass into ring slot s
-    auto issue_rows = [&](const int4& item, int pass, int rows, int ks, int s) {
+    auto issue_rows = [&](const SItem& item, int pass, int rows, int ks, int s) {
       const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
       const uint32_t xbytes = units * kUnitK * 2;
       uint8_t* st = smem + s * Cfg::kStageBytes;
       for (int j = lane; j < rows; j += 32) {
-        const int r = item.z + pass * Cfg::kRowsPerPass + j;
+        const int r = item.row0 + pass * Cfg::kRowsPerPass + j;
         const int row = GATHER ? ld_map(a.sorted + r, how) / a.topk : r;
         const uint16_t* src = a.A + static_cast<size_t>(row) * a.K + ks * kUnitsPerStage * kUnitK;
         bulk_g2s(st + Cfg::kWBytes + j * kXPitch, src, xbytes, &full_bar[s]);
       }
     };
     int nblocks = 0;
-    int4 first = make_int4(0, 0, 0, -1);
+    SItem first{0, 0, 0, -1, 0, 0, 0, 0};
     int pre = 0;   // stages of the first item's first pass already issued
     if (a.pdl == 2) {
       // The expert map is read from L2 here, never from a copy an SM cached
@@ -260,25 +285,36 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       set_status(a.status, CHORD_ERR_INVALID_ARG);
       nblocks = nblocks < 0 ? 0 : a.max_blocks;
     }
-    const long long total = static_cast<long long>(a.n_tiles) * nblocks;
+    // split-K when the grid is not saturated: at most half as many items
+    // as CTAs, one pass per item, a split workspace and more than one stage
+    const long long n_base = static_cast<long long>(a.n_tiles) * nblocks;
+    int nsplit = 1;
+    if (a.partial && a.block_m <= Cfg::kRowsPerPass && k_stages > 1 && n_base > 0 &&
+        2 * n_base <= static_cast<long long>(gridDim.x)) {
+      nsplit = static_cast<int>(min(static_cast<long long>(gridDim.x) / n_base,
+                                    static_cast<long long>(min(k_stages, kMaxSplit))));
+      nsplit = static_cast<int>(min(static_cast<long long>(nsplit), kSplitSlots / n_base));
+      if (nsplit < 2) nsplit = 1;
+    }
+    const long long total = n_base * nsplit;
     if (a.pdl == 2) {
       int i = 0;
       if (lane == 0) i = atomicAdd(a.work, 1);
       i = __shfl_sync(0xffffffffu, i, 0);
-      first = decode_item(i, total, nblocks, 2);
-      const int rows0 = min(Cfg::kRowsPerPass, first.w);
+      first = decode_item(i, total, nblocks, nsplit, 2);
+      const int rows0 = min(Cfg::kRowsPerPass, first.rows);
       if (rows0 > 0) {
-        pre = min(STAGES, k_stages);
-        for (int ks = 0; ks < pre; ++ks) issue_weights(weight_tile(first), rows0, ks, ks);
+        pre = min(STAGES, first.ks1 - first.ks0);
+        for (int j = 0; j < pre; ++j) issue_weights(weight_tile(first), rows0, first.ks0 + j, j);
       }
       grid_dep_wait();
       grid_dep_launch();
-      for (int ks = 0; ks < pre; ++ks) issue_rows(first, 0, rows0, ks, ks);
+      for (int j = 0; j < pre; ++j) issue_rows(first, 0, rows0, first.ks0 + j, j);
     }
     int it = 0, q = 0;
     bool ok = true, use_first = a.pdl == 2;
     while (ok) {
-      int4 item;
+      SItem item;
       if (use_first) {   // fetched before the wait
         item = first;
         use_first = false;
@@ -286,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
         int i = 0;
         if (lane == 0) i = atomicAdd(a.work, 1);
         i = __shfl_sync(0xffffffffu, i, 0);
-        item = decode_item(i, total, nblocks, how);
+        item = decode_item(i, total, nblocks, nsplit, how);
       }
       const int slot = q % kItemSlots;
       if (q >= kItemSlots)
@@ -298,13 +334,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
         mbar_arrive(&item_full[slot]);
       }
       ++q;
-      if (item.w < 0) break;
+      if (item.rows < 0) break;
       const uint8_t* wtile = weight_tile(item);
-      const int passes = (item.w + Cfg::kRowsPerPass - 1) / Cfg::kRowsPerPass;
+      const int passes = (item.rows + Cfg::kRowsPerPass - 1) / Cfg::kRowsPerPass;
       for (int pass = 0; pass < passes && ok; ++pass) {
-        const int rows = min(Cfg::kRowsPerPass, item.w - pass * Cfg::kRowsPerPass);
-        for (int ks = 0; ks < k_stages; ++ks, ++it) {
-          if (pre > 0) {   // issued before the wait (first pass of the first item: it == ks)
+        const int rows = min(Cfg::kRowsPerPass, item.rows - pass * Cfg::kRowsPerPass);
+        for (int ks = item.ks0; ks < item.ks1; ++ks, ++it) {
+          if (pre > 0) {   // issued before the wait (first pass of the first item: it == ks - ks0)
             --pre;
             continue;
           }
@@ -341,20 +377,21 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
   for (int q = 0;; ++q) {
     const int slot = q % kItemSlots;
     if (!mbar_wait(&item_full[slot], (q / kItemSlots) & 1, a.status)) return;
-    const int4 item = item_q[slot];
+    const SItem item = item_q[slot];
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[slot]);
-    if (item.w < 0) return;
-    const int passes = (item.w + Cfg::kRowsPerPass - 1) / Cfg::kRowsPerPass;
+    if (item.rows < 0) return;
+    const int passes = (item.rows + Cfg::kRowsPerPass - 1) / Cfg::kRowsPerPass;
+    const int sp = item.split & 0xffff, nsplit = item.split >> 16;
     for (int pass = 0; pass < passes; ++pass) {
-      const int rows = min(Cfg::kRowsPerPass, item.w - pass * Cfg::kRowsPerPass);
+      const int rows = min(Cfg::kRowsPerPass, item.rows - pass * Cfg::kRowsPerPass);
       float acc[NT][4];
 #pragma unroll
       for (int n = 0; n < NT; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
 
-      for (int ks = 0; ks < k_stages; ++ks, ++it) {
+      for (int ks = item.ks0; ks < item.ks1; ++ks, ++it) {
         const int s = it % STAGES;
         if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status)) return;
         const uint32_t st = smem_base + s * Cfg::kStageBytes;
@@ -372,8 +409,48 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
         if (lane == 0) mbar_arrive(&empty_bar[s]);
       }
 
+      if (nsplit > 1) {
+        // split-K (one pass per item): publish this split's partial, and
+        // the last split of the item to arrive adds all of them in split
+        // order and runs the epilogue
+        float* slot_base = a.partial + static_cast<size_t>(item.base) * nsplit * kSplitSlotFloats;
+        float4* mine = reinterpret_cast<float4*>(slot_base + static_cast<size_t>(sp) * kSplitSlotFloats +
+                                                 (warp * 32 + lane) * 4 * NT);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) mine[n] = make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(a.split_cnt + item.base * kConsumerWarps + warp, 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev != nsplit - 1) continue;   // not the last split of this item
+        __threadfence();
+        if (lane == 0) atomicExch(a.split_cnt + item.base * kConsumerWarps + warp, 0);   // ready for the next launch
+        float sum[NT][4];
+        for (int k = 0; k < nsplit; ++k) {
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            float4 v;
+            if (k == sp) {
+              v = make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
+            } else {
+              v = ld_cg_f4(slot_base + static_cast<size_t>(k) * kSplitSlotFloats + (warp * 32 + lane) * 4 * NT + 4 * n);
+            }
+            if (k == 0) {
+              sum[n][0] = v.x; sum[n][1] = v.y; sum[n][2] = v.z; sum[n][3] = v.w;
+            } else {
+              sum[n][0] += v.x; sum[n][1] += v.y; sum[n][2] += v.z; sum[n][3] += v.w;
+            }
+          }
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[n][i] = sum[n][i];
+      }
+
       // ---------------------------------------------------------- epilogue
-      const size_t r0 = static_cast<size_t>(item.z) + pass * Cfg::kRowsPerPass;
+      const size_t r0 = static_cast<size_t>(item.row0) + pass * Cfg::kRowsPerPass;
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
 #pragma unroll
@@ -383,10 +460,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
           uint16_t* crow = a.C + (r0 + tok) * a.ldc;
           if (EPI == CHORD_EPI_SILU_MUL) {
             // acc[n][i]: gate of index i0 + g; acc[n][2 + i]: up of the same index
-            const int col = 32 * item.x + 8 * warp + g;
+            const int col = 32 * item.tile + 8 * warp + g;
             crow[col] = f32_to_bf16_rn(silu_f32(acc[n][i]) * acc[n][2 + i]);
           } else {
-            const int col = kTileRows * item.x + 16 * warp + g;
+            const int col = kTileRows * item.tile + 16 * warp + g;
             if (col < a.N) crow[col] = f32_to_bf16_rn(acc[n][i]);
             if (col + 8 < a.N) crow[col + 8] = f32_to_bf16_rn(acc[n][2 + i]);
           }
@@ -450,6 +527,8 @@ cudaError_t gemm_small_launch(const GemmLaunch& g, int rows_per_pass, cudaStream
   a.E_local = g.E_local;
   a.pdl = g.pdl;
   a.max_blocks = g.max_blocks;
+  a.partial = g.split_cnt ? g.split_partial : nullptr;
+  a.split_cnt = g.split_cnt;
   const PackHeader h = make_pack_header(g.E_local, g.N, g.K, g.epilogue == CHORD_EPI_SILU_MUL);
   a.n_tiles = h.n_tiles;
   a.tile_bytes = h.tile_bytes;

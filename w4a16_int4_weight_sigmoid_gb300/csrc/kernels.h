@@ -55,6 +55,11 @@ struct GemmLaunch {
   // before the wait (the previous kernel is a GEMM launched with mode 1).
   int pdl = 0;
   int max_blocks = 0;   // BLOCK_M blocks the aligned buffers hold (capacity / block_m)
+  // Split-K workspace of the small-M path (kSplitPartialBytes of partials,
+  // kSplitCntBytes of counters that are zero between launches); NULL: the
+  // kernel never splits K.
+  float* split_partial = nullptr;
+  int* split_cnt = nullptr;
 };
 // Dense GEMM: one-expert block map (counts, offsets, ntpp, expert_ids) for M rows.
 cudaError_t dense_setup_launch(int M, int bm, int32_t* counts, int32_t* offsets, int32_t* ntpp,
