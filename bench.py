@@ -677,20 +677,26 @@ def run_report(args):
             y = torch.empty((rows_n, H), dtype=torch.bfloat16, device=dev)
             ws = torch.zeros(chord.chord_w4a16_grouped_workspace_bytes(E, rows_n), dtype=torch.uint8, device=dev)
             st = torch.zeros(1, dtype=torch.int32, device=dev)
-            for name, A, W, N, K, epi, C in (("gate_up", x, layer.w13, 2 * I, H, chord.CHORD_EPI_SILU_MUL, h),
-                                             ("down", h, layer.w2, H, I, chord.CHORD_EPI_STORE, y)):
+            for (name, A, W, N, K, epi, C), path in [
+                    (gm, p) for gm in (("gate_up", x, layer.w13, 2 * I, H, chord.CHORD_EPI_SILU_MUL, h),
+                                       ("down", h, layer.w2, H, I, chord.CHORD_EPI_STORE, y))
+                    for p in (chord.CHORD_PATH_SMALL_M, chord.CHORD_PATH_LARGE_M, chord.CHORD_PATH_AUTO)]:
+                tun = chord.chord_tuning(path, 0, 0, 0)
                 if layout == "masked":
-                    f = lambda A=A, W=W, N=N, K=K, epi=epi, C=C: chord.chord_w4a16_grouped_gemm_masked(
-                        A.view(E, per_e, K), g, W, N, K, epi, C.view(E, per_e, -1), ws, per_e, dev_status=st)
+                    f = lambda A=A, W=W, N=N, K=K, epi=epi, C=C, tun=tun: chord.chord_w4a16_grouped_gemm_masked(
+                        A.view(E, per_e, K), g, W, N, K, epi, C.view(E, per_e, -1), ws, per_e, tuning=tun,
+                        dev_status=st)
                 else:
-                    f = lambda A=A, W=W, N=N, K=K, epi=epi, C=C: chord.chord_w4a16_grouped_gemm_contiguous(
-                        A, g, W, N, K, epi, C, ws, per_e, dev_status=st)
+                    f = lambda A=A, W=W, N=N, K=K, epi=epi, C=C, tun=tun: chord.chord_w4a16_grouped_gemm_contiguous(
+                        A, g, W, N, K, epi, C, ws, per_e, tuning=tun, dev_status=st)
                 us = graph_us([f], reps_in_graph=10, replays=20)
                 byts = wbytes[name] + rows_n * K * 2 + rows_n * (N // 2 if epi == chord.CHORD_EPI_SILU_MUL else N) * 2
                 flops = 2.0 * rows_n * N * K
                 t_hbm, t_tc = byts / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops_sustained"] * 1e12)
                 bound = "hbm" if t_hbm >= t_tc else "tensor"
                 rows.append({"layout": layout, "rows_per_expert": per_e, "gemm": name, "us": round(us, 2),
+                             "path": {chord.CHORD_PATH_SMALL_M: "register-mma", chord.CHORD_PATH_LARGE_M: "tcgen05",
+                                      chord.CHORD_PATH_AUTO: "auto"}[path],
                              "bound": bound, "frac": round(max(t_hbm, t_tc) / (us * 1e-6), 4),
                              "achieved": round(byts / (us * 1e-6) / 1e9, 1) if bound == "hbm"
                              else round(flops / (us * 1e-6) / 1e12, 1),

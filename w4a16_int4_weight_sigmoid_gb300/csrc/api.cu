@@ -56,6 +56,11 @@ int rows_per_pass_for(double tok_e) {
 // or above which the tensor-core (tcgen05) path is used; [Chord] "인덱스 커널
 // 기법" switches schedules around 80 rows per expert.
 constexpr double kLargeTokE = 64.0;
+// The grouped and dense entry points know the rows per expert themselves
+// (expected_m, or M): measured on GB300 with the masked layout at 32 rows
+// per expert over 48 Kimi EP8 experts, the tcgen05 path took 305 / 162 us
+// (gate/up / down) against 358 / 192 us on the register path.
+constexpr double kGroupedLargeTokE = 16.0;
 // chord_moe_layer's policy: expected rows per expert M*topk/E_total at or
 // above which the tcgen05 path is used.  Measured on GB300 at Kimi EP8
 // shapes (whole layer, both paths forced, split-K decode GEMM and two
@@ -429,7 +434,7 @@ int grouped_impl(const chord_bf16* A, size_t capacity, const int32_t* group_rows
   if (ws_bytes < need) return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "grouped GEMM workspace %zu < %zu", ws_bytes, need);
   chord_tuning plan{};
   if (tuning) plan = *tuning;
-  if (!plan.path) plan.path = (tok_e >= kLargeTokE && N % 128 == 0) ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
+  if (!plan.path) plan.path = (tok_e >= kGroupedLargeTokE && N % 128 == 0) ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
   if (!plan.rows_per_pass) plan.rows_per_pass = rows_per_pass_for(tok_e);
   if (plan.path == CHORD_PATH_LARGE_M && N % 128 != 0)   // checked before anything is launched
     return fail(CHORD_ERR_UNSUPPORTED, "tcgen05 path needs N %% 128 == 0");
@@ -536,7 +541,7 @@ int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, in
   chord_tuning plan{};
   if (tuning) plan = *tuning;
   if (!plan.path)
-    plan.path = (tok_e >= kLargeTokE && N % 128 == 0) ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
+    plan.path = (tok_e >= kGroupedLargeTokE && N % 128 == 0) ? CHORD_PATH_LARGE_M : CHORD_PATH_SMALL_M;
   if (!plan.rows_per_pass) plan.rows_per_pass = rows_per_pass_for(tok_e);
   if (plan.path == CHORD_PATH_LARGE_M && N % 128 != 0)   // checked before anything is launched
     return fail(CHORD_ERR_UNSUPPORTED, "tcgen05 path needs N %% 128 == 0");

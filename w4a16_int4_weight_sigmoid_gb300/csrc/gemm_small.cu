@@ -69,7 +69,8 @@ constexpr int kMaxSplit = 8;
 
 // A work item as the producer hands it to the consumers.  rows = -1: end.
 struct SItem {
-  int tile, e, row0, rows;   // 64-row weight tile, local expert, first sorted row, rows of the block
+  int tile, e, row0, rows;   // first 64-row weight tile, local expert, first sorted row, rows of the block
+  int ntl;                   // consecutive weight tiles in the item (several only when K fits one stage)
   int ks0, ks1;              // K stages [ks0, ks1) of this split
   int base;                  // item index without the split (counter index)
   int split;                 // split index | (number of splits << 16)
@@ -197,6 +198,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
 
   const int n_units = a.K / kUnitK;
   const int k_stages = (n_units + kUnitsPerStage - 1) / kUnitsPerStage;
+  // Short K (one stage per tile): an item covers as many consecutive weight
+  // tiles as fill a stage (2 at K = 256, 4 at K = 128), so each mbarrier
+  // hand-off carries a full stage of weights and the block's activation
+  // rows are loaded once for all of them.
+  const int tpi = k_stages == 1 ? max(1, kUnitsPerStage / n_units) : 1;
+  const int n_groups = (a.n_tiles + tpi - 1) / tpi;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -223,12 +230,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     const int how = a.pdl ? 1 : 0;   // after the wait
     // item i -> split s of base item i / S = (tile, block), block index fastest
     auto decode_item = [&](int i, long long total, int nblocks, int nsplit, int how) {
-      SItem item{0, 0, 0, -1, 0, 0, 0, 0};
+      SItem item{0, 0, 0, -1, 1, 0, 0, 0, 0};
       if (i < total) {
         const int base = i / nsplit, sp = i - base * nsplit;
-        const int nt = base / nblocks, b = base - nt * nblocks;
+        const int ng = base / nblocks, b = base - ng * nblocks;
         const int e = ld_map(a.expert_ids + b, how);
-        item = SItem{nt, 0, 0, 0, sp * k_stages / nsplit, (sp + 1) * k_stages / nsplit, base, sp | (nsplit << 16)};
+        item = SItem{ng * tpi, 0, 0, 0, min(tpi, a.n_tiles - ng * tpi), sp * k_stages / nsplit,
+                     (sp + 1) * k_stages / nsplit, base, sp | (nsplit << 16)};
         if (e >= 0 && e < a.E_local) {
           const int row0 = b * a.block_m;
           const int end = ld_map(a.offsets + e, how) + ld_map(a.counts + e, how);
@@ -246,12 +254,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
              (static_cast<size_t>(item.e) * a.n_tiles + item.tile) * static_cast<size_t>(a.tile_bytes);
     };
     // weights of stage ks into ring slot s, the slot expecting `rows` rows too
-    auto issue_weights = [&](const uint8_t* wtile, int rows, int ks, int s) {
+    // weights of stage ks into ring slot s, the slot expecting `rows` rows
+    // too; an item of ntl > 1 tiles (one stage each) copies all of them
+    auto issue_weights = [&](const uint8_t* wtile, int ntl, int rows, int ks, int s) {
       const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
       if (lane == 0) {
-        mbar_arrive_expect_tx(&full_bar[s], units * kUnitBytes + rows * units * kUnitK * 2);
+        mbar_arrive_expect_tx(&full_bar[s], ntl * units * kUnitBytes + rows * units * kUnitK * 2);
         bulk_g2s(smem + s * Cfg::kStageBytes, wtile + static_cast<size_t>(ks) * kUnitsPerStage * kUnitBytes,
-                 units * kUnitBytes, &full_bar[s]);
+                 ntl * units * kUnitBytes, &full_bar[s]);
       }
       __syncwarp();
     };
@@ -268,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       }
     };
     int nblocks = 0;
-    SItem first{0, 0, 0, -1, 0, 0, 0, 0};
+    SItem first{0, 0, 0, -1, 1, 0, 0, 0, 0};
     int pre = 0;   // stages of the first item's first pass already issued
     if (a.pdl == 2) {
       // The expert map is read from L2 here, never from a copy an SM cached
@@ -287,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     }
     // split-K when the grid is not saturated: at most half as many items
     // as CTAs, one pass per item, a split workspace and more than one stage
-    const long long n_base = static_cast<long long>(a.n_tiles) * nblocks;
+    const long long n_base = static_cast<long long>(n_groups) * nblocks;
     int nsplit = 1;
     if (a.partial && a.block_m <= Cfg::kRowsPerPass && k_stages > 1 && n_base > 0 &&
         2 * n_base <= static_cast<long long>(gridDim.x)) {
@@ -305,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       const int rows0 = min(Cfg::kRowsPerPass, first.rows);
       if (rows0 > 0) {
         pre = min(STAGES, first.ks1 - first.ks0);
-        for (int j = 0; j < pre; ++j) issue_weights(weight_tile(first), rows0, first.ks0 + j, j);
+        for (int j = 0; j < pre; ++j) issue_weights(weight_tile(first), first.ntl, rows0, first.ks0 + j, j);
       }
       grid_dep_wait();
       grid_dep_launch();
@@ -348,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
           if (it >= STAGES) ok = mbar_wait_backoff(&empty_bar[s], ((it / STAGES) - 1) & 1, a.status);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
-          issue_weights(wtile, rows, ks, s);
+          issue_weights(wtile, item.ntl, rows, ks, s);
           issue_rows(item, pass, rows, ks, s);
         }
       }
@@ -383,6 +393,51 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     if (item.rows < 0) return;
     const int passes = (item.rows + Cfg::kRowsPerPass - 1) / Cfg::kRowsPerPass;
     const int sp = item.split & 0xffff, nsplit = item.split >> 16;
+    // BF16 output of one 64-row weight tile for `rows` token rows from r0
+    auto epilogue = [&](int tile, const float (&acc)[NT][4], int rows, size_t r0) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int tok = n * 8 + 2 * t + i;
+          if (tok >= rows) continue;
+          uint16_t* crow = a.C + (r0 + tok) * a.ldc;
+          if (EPI == CHORD_EPI_SILU_MUL) {
+            // acc[n][i]: gate of index i0 + g; acc[n][2 + i]: up of the same index
+            const int col = 32 * tile + 8 * warp + g;
+            crow[col] = f32_to_bf16_rn(silu_f32(acc[n][i]) * acc[n][2 + i]);
+          } else {
+            const int col = kTileRows * tile + 16 * warp + g;
+            if (col < a.N) crow[col] = f32_to_bf16_rn(acc[n][i]);
+            if (col + 8 < a.N) crow[col + 8] = f32_to_bf16_rn(acc[n][2 + i]);
+          }
+        }
+      }
+    };
+    if (item.ntl > 1) {
+      // several tiles, one stage (K <= 512): per pass, tile by tile
+      for (int pass = 0; pass < passes; ++pass, ++it) {
+        const int rows = min(Cfg::kRowsPerPass, item.rows - pass * Cfg::kRowsPerPass);
+        const int s = it % STAGES;
+        if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status)) return;
+        const uint32_t st = smem_base + s * Cfg::kStageBytes;
+#pragma unroll 1
+        for (int tl = 0; tl < item.ntl; ++tl) {
+          float acc[NT][4];
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
+#pragma unroll 1
+          for (int u = 0; u < n_units; ++u)
+            unit_mma<NT>(st + (tl * n_units + u) * kUnitBytes, st + x_off + u * kUnitK * 2, q_off, s_off, a, acc);
+          epilogue(item.tile + tl, acc, rows, static_cast<size_t>(item.row0) + pass * Cfg::kRowsPerPass);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
+      continue;
+    }
     for (int pass = 0; pass < passes; ++pass) {
       const int rows = min(Cfg::kRowsPerPass, item.rows - pass * Cfg::kRowsPerPass);
       float acc[NT][4];
@@ -449,26 +504,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
           for (int i = 0; i < 4; ++i) acc[n][i] = sum[n][i];
       }
 
-      // ---------------------------------------------------------- epilogue
-      const size_t r0 = static_cast<size_t>(item.row0) + pass * Cfg::kRowsPerPass;
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int tok = n * 8 + 2 * t + i;
-          if (tok >= rows) continue;
-          uint16_t* crow = a.C + (r0 + tok) * a.ldc;
-          if (EPI == CHORD_EPI_SILU_MUL) {
-            // acc[n][i]: gate of index i0 + g; acc[n][2 + i]: up of the same index
-            const int col = 32 * item.tile + 8 * warp + g;
-            crow[col] = f32_to_bf16_rn(silu_f32(acc[n][i]) * acc[n][2 + i]);
-          } else {
-            const int col = kTileRows * item.tile + 16 * warp + g;
-            if (col < a.N) crow[col] = f32_to_bf16_rn(acc[n][i]);
-            if (col + 8 < a.N) crow[col + 8] = f32_to_bf16_rn(acc[n][2 + i]);
-          }
-        }
-      }
+      epilogue(item.tile, acc, rows, static_cast<size_t>(item.row0) + pass * Cfg::kRowsPerPass);
     }
   }
 }
