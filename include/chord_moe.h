@@ -55,8 +55,10 @@ enum chord_status {
 
 /* GEMM epilogues. */
 enum chord_epilogue {
-  CHORD_EPI_STORE = 0,    /* C[r, n] = bf16(acc[r, n]) */
-  CHORD_EPI_SILU_MUL = 1  /* C[r, i] = bf16(silu(acc[r, i]) * acc[r, I + i]), I = N/2 */
+  CHORD_EPI_STORE = 0,        /* C[r, n] = bf16(acc[r, n]) */
+  CHORD_EPI_SILU_MUL = 1,     /* C[r, i] = bf16(silu(acc[r, i]) * acc[r, I + i]), I = N/2 */
+  CHORD_EPI_WEIGHTED_ADD = 2  /* FP32 C[t, n] += topk_weights[f] * acc[r, n], f = sorted_token_ids[r],
+                                 t = f / topk (indexed GEMM only; see chord_w4a16_moe_gemm) */
 };
 
 /* GEMM execution paths. */
@@ -80,6 +82,14 @@ typedef struct chord_tuning {
 
 /* Description of the last failure on the calling thread ("" if none). */
 const char* chord_last_error_string(void);
+/* Test hook for the device timeout path, not needed in normal use: while
+ * enabled, every later launch of the register-MMA GEMM in this process
+ * withholds its work items from its consumer warps (the producer issues no
+ * copy and hands out no item), so the consumers' barrier waits run out after
+ * a short limit: the kernel records CHORD_ERR_TIMEOUT in dev_status and
+ * returns, with no copy in flight and the work-queue counters left zero.
+ * Nothing is computed.  enable = 0 turns it off.  Returns CHORD_OK. */
+int chord_debug_force_timeout(int enable);
 /* Library version, major*10000 + minor*100 + patch. */
 int chord_version(void);
 
@@ -224,7 +234,18 @@ int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E,
  *            CHORD_ERR_INVALID_ARG / CHORD_ERR_ROUTING_INVALID) but do not
  *            re-check every row index against these buffers.
  *   C        BF16 [capacity, N] (STORE) or [capacity, N/2] (SILU_MUL); padding
- *            rows are not written
+ *            rows are not written.  CHORD_EPI_WEIGHTED_ADD ([HumPR] "왜 이게
+ *            좋은가" 3, moe_fused_mul_sum: the weight multiply and the sum
+ *            fused into the GEMM): C is an FP32 [M, N] token-major
+ *            accumulator that the caller initialises (zeros, or a partial
+ *            sum to add to); every valid row r adds topk_weights[f] *
+ *            acc[r, :] to C[f / topk, :] with FP32 atomic adds, f =
+ *            sorted_token_ids[r].  The additions of a token's rows happen in
+ *            no fixed order, so the low bits of the sum may differ from call
+ *            to call; chord_moe_sum is the deterministic alternative.
+ *            Needs a_gather = 0 and topk_weights.
+ *   topk_weights  FP32 [M, topk] routing weights (CHORD_EPI_WEIGHTED_ADD
+ *            only; may be NULL otherwise)
  *   workspace  chord_w4a16_moe_gemm_workspace_bytes() bytes, 16-byte aligned;
  *            zero it once when it is allocated.  Layout: 256 bytes of
  *            work-queue counters, then the split-K area (arrival counters
@@ -232,7 +253,9 @@ int chord_w4a16_prepack(const uint8_t* qweight, const chord_bf16* scales, int E,
  *            on the tensor-core path, the gathered rows.  Every call leaves
  *            the counters zero (the last CTA of a launch resets the queue,
  *            also after a device timeout; the last split of an item resets
- *            its counter).
+ *            its counter).  After a call that recorded CHORD_ERR_TIMEOUT a
+ *            split item may have lost its last split: zero the workspace
+ *            again before reusing it.
  *   dev_status  device int for errors found on the device (may be NULL)
  * Two paths ([Humming] "워크로드별 튜닝 및 JIT 컴파일": async-copy + MMA at
  * small batch, TMA + UMMA at large batch), chosen from the expected rows per
@@ -252,8 +275,9 @@ int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w
                          int N, int K, int M, int topk, const int32_t* sorted_token_ids,
                          const int32_t* expert_ids, const int32_t* num_tokens_post_padded,
                          const int32_t* expert_counts, const int32_t* expert_offsets, int block_m,
-                         size_t capacity, int epilogue, chord_bf16* C, const chord_tuning* tuning,
-                         void* workspace, size_t ws_bytes, int* dev_status, void* stream);
+                         size_t capacity, int epilogue, const float* topk_weights, void* C,
+                         const chord_tuning* tuning, void* workspace, size_t ws_bytes, int* dev_status,
+                         void* stream);
 
 /* ------------------------------------------------------- dense W4A16 GEMM
  * C = A * (q*s)^T for one weight matrix, no routing: the indexed GEMM above

@@ -98,27 +98,27 @@ def test_argument_checks_reject_before_launch(L):
     rc, _ = _rc_and_msg(L, L.chord_w4a16_prepack(P, P, 2, 96, 128, 32, 1, P, 10 ** 9, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # gate_up needs N % 64
     t = chord.chord_tuning(0, 0, 1, 0)
-    rc, msg = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 0,
+    rc, msg = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 0, None,
                                                     P, ctypes.byref(t), P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_UNSUPPORTED and "FP16" in msg
     t = chord.chord_tuning(0, 0, 0, 1)
-    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 0,
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 0, None,
                                                   P, ctypes.byref(t), P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_UNSUPPORTED
-    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 100, 8, 2, P, P, P, P, P, 16, 100, 0,
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 100, 8, 2, P, P, P, P, P, 16, 100, 0, None,
                                                   P, None, P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # K % 64
-    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 96, 128, 8, 2, P, P, P, P, P, 16, 100, 1,
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 96, 128, 8, 2, P, P, P, P, P, 16, 100, 1, None,
                                                   P, None, P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # SiLU needs N % 64
-    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 12, 100, 0,
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 12, 100, 0, None,
                                                   P, None, P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_INVALID_ARG                        # block_m
-    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 0,
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 0, None,
                                                   P, None, P, 100, None, None))
     assert rc == chord.CHORD_ERR_WORKSPACE_TOO_SMALL                # < counters + split-K area
     t = chord.chord_tuning(chord.CHORD_PATH_LARGE_M, 0, 0, 0)
-    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 192, 128, 8, 2, P, P, P, P, P, 16, 100, 0,
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 192, 128, 8, 2, P, P, P, P, P, 16, 100, 0, None,
                                                   P, ctypes.byref(t), P, 1 << 24, None, None))
     assert rc == chord.CHORD_ERR_UNSUPPORTED                        # tcgen05 path needs N % 128
     rc, _ = _rc_and_msg(L, L.chord_moe_sum(P, P, P, 4, 2, 100, P, None))
@@ -159,6 +159,29 @@ def test_new_entry_points_reject_before_launch(L):
     t = chord.chord_tuning(chord.CHORD_PATH_LARGE_M, 0, 0, 0)
     rc, _ = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 192, 128, 1000, 0, P, ctypes.byref(t), P, need, None, None))
     assert rc == chord.CHORD_ERR_UNSUPPORTED
+
+
+def test_weighted_add_epilogue_checks(L):
+    """CHORD_EPI_WEIGHTED_ADD reads rows in sorted order and needs the routing
+    weights; the dense and grouped GEMMs, which have no routing, refuse it."""
+    P = ctypes.c_void_p(16)
+    WADD = chord.CHORD_EPI_WEIGHTED_ADD
+    big = 1 << 24
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 1, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, WADD, P,
+                                                  P, None, P, big, None, None))
+    assert rc == chord.CHORD_ERR_UNSUPPORTED                        # gathered rows
+    rc, msg = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 0, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, WADD, None,
+                                                    P, None, P, big, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "topk_weights" in msg
+    rc, msg = _rc_and_msg(L, L.chord_w4a16_gemm(P, P, 256, 128, 8, WADD, P, None, P, big, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "routing" in msg
+    need = L.chord_w4a16_grouped_workspace_bytes(8, 1024)
+    rc, msg = _rc_and_msg(L, L.chord_w4a16_grouped_gemm_contiguous(P, 1024, P, 8, 0, P, 256, 128, WADD, P, None,
+                                                                   P, need, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG and "routing" in msg
+    rc, _ = _rc_and_msg(L, L.chord_w4a16_moe_gemm(P, 0, P, 4, 256, 128, 8, 2, P, P, P, P, P, 16, 100, 3, P,
+                                                  P, None, P, big, None, None))
+    assert rc == chord.CHORD_ERR_INVALID_ARG                        # unknown epilogue
 
 
 def test_grouped_entry_points_reject_before_launch(L):

@@ -214,3 +214,40 @@ def test_gemm_split_k_counters_and_parity():
             assert_close_to_oracle(outs[-1][rows], ref, f"split-K expert {e}", *GEMM_TOL[SMALL])
     n = al["num_tokens_post_padded"]
     assert np.array_equal(outs[0][:n].view(np.uint16), outs[1][:n].view(np.uint16))
+
+
+@pytest.mark.parametrize("path", [SMALL, LARGE])
+@pytest.mark.parametrize("M,K,N,E,topk,bm", [(40, 256, 384, 6, 3, 16), (300, 512, 256, 4, 2, 16)])
+def test_weighted_add_epilogue(path, M, K, N, E, topk, bm):
+    """CHORD_EPI_WEIGHTED_ADD: the down GEMM over rows in sorted order adds
+    topk_weights[f] * row into token f / topk of an FP32 [M, N] accumulator.
+    Expected: for every token, the sum over its local assignments of w times
+    the oracle's expert GEMM row (FP64).  The accumulator starts from a
+    known non-zero value, which the epilogue must add to, not overwrite."""
+    logits, bias = wl.router_inputs(M, E, 61)
+    w, ids, _ = oracle.route(logits, bias, topk)
+    al = oracle.moe_align(ids, 0, E, bm)
+    up = _upload_align(al, M, topk, E, bm)
+    cap = up[0]
+    A = wl.activations(cap, K, 62)           # one row per sorted row (the gate/up output)
+    q = wl.int4_weights(E, N, K, 63, wl.S_Q2)
+    s = wl.group_scales(E, N, K, 64, wl.S_S2)
+    packed = prepack(to_device(q), to_device(s), False)
+    rows = _oracle_rows(A, q, s, al, topk, STORE, False)
+    ref = np.full((M, N), 0.25)
+    st = al["sorted_token_ids"]
+    for e, (r, vals) in rows.items():
+        for k, row in enumerate(r):
+            f = int(st[row])
+            ref[f // topk] += float(w.ravel()[f]) * vals[k]
+    ws = torch.zeros(chord.chord_w4a16_moe_gemm_workspace_bytes(cap, K, False), dtype=torch.uint8, device="cuda")
+    tw = torch.from_numpy(np.ascontiguousarray(w, np.float32)).cuda()
+    C = torch.full((M, N), 0.25, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    chord.chord_w4a16_moe_gemm(to_device(A), False, packed, E, N, K, M, topk, *up[1:], bm,
+                               chord.CHORD_EPI_WEIGHTED_ADD, C, ws, tuning=chord.chord_tuning(path, 0, 0, 0),
+                               dev_status=status, topk_weights=tw)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert int(ws[:256].view(torch.int32).abs().sum().item()) == 0
+    assert_close_to_oracle(C.cpu().numpy().astype(np.float64), ref, f"weighted add path {path}", *GEMM_TOL[path])

@@ -26,6 +26,7 @@ CHORD_ERR_ROUTING_INVALID = -7
 
 CHORD_EPI_STORE = 0
 CHORD_EPI_SILU_MUL = 1
+CHORD_EPI_WEIGHTED_ADD = 2
 
 CHORD_PATH_AUTO = 0
 CHORD_PATH_SMALL_M = 1
@@ -49,6 +50,7 @@ _Z = ctypes.c_size_t
 _SIGS = {
     "chord_last_error_string": (ctypes.c_char_p, []),
     "chord_version": (_I, []),
+    "chord_debug_force_timeout": (_I, [_I]),
     "chord_moe_route": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "chord_moe_align_capacity": (_Z, [_I, _I, _I, _I]),
     "chord_moe_align_workspace_bytes": (_Z, [_I, _I, _I]),
@@ -60,7 +62,7 @@ _SIGS = {
     "chord_w4a16_prepack": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "chord_w4a16_moe_gemm_workspace_bytes": (_Z, [_Z, _I, _I]),
     "chord_w4a16_moe_gemm": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _Z, _I,
-                                  _P, _P, _P, _Z, _P, _P]),
+                                  _P, _P, _P, _P, _Z, _P, _P]),
     "chord_moe_sum": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "chord_w4a16_gemm_workspace_bytes": (_Z, [_I]),
     "chord_w4a16_gemm": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P, _P]),
@@ -151,6 +153,12 @@ def chord_version() -> int:
     return lib().chord_version()
 
 
+def chord_debug_force_timeout(enable: bool) -> None:
+    """Test hook: later register-MMA GEMM launches withhold their work items,
+    so their consumers' waits run out (CHORD_ERR_TIMEOUT, nothing computed)."""
+    _check(lib().chord_debug_force_timeout(int(bool(enable))))
+
+
 def chord_moe_route(logits, bias, topk: int, topk_weights, topk_ids, stream=None):
     M, E = logits.shape
     _check(lib().chord_moe_route(_ptr(logits, torch.float32, "logits"), _ptr(bias, torch.float32, "bias"),
@@ -232,11 +240,19 @@ def chord_w4a16_moe_gemm_workspace_bytes(capacity: int, K: int, a_gather: bool) 
 def chord_w4a16_moe_gemm(A, a_gather: bool, packed_w, E_local: int, N: int, K: int, M: int,
                          topk: int, sorted_token_ids, expert_ids, num_tokens_post_padded,
                          expert_counts, expert_offsets, block_m: int, epilogue: int, C, workspace,
-                         tuning=None, dev_status=None, stream=None):
-    """workspace: uint8 tensor of chord_w4a16_moe_gemm_workspace_bytes() bytes whose first
-    256 bytes were zeroed once (the library keeps them zero)."""
+                         tuning=None, dev_status=None, stream=None, topk_weights=None):
+    """workspace: uint8 tensor of chord_w4a16_moe_gemm_workspace_bytes() bytes, zeroed once
+    when allocated (the library keeps its counters zero).  CHORD_EPI_WEIGHTED_ADD: C is a
+    float32 [M, N] accumulator the caller initialises, topk_weights float32 [M, topk]."""
     cap = sorted_token_ids.numel()
-    _check_operands(A, C, K, N, epilogue, M if a_gather else cap, cap, "chord_w4a16_moe_gemm")
+    if epilogue == CHORD_EPI_WEIGHTED_ADD:
+        if not isinstance(C, torch.Tensor) or C.dtype != torch.float32 or C.numel() < M * N:
+            raise ValueError("chord_w4a16_moe_gemm: the weighted add needs a float32 C of M x N values")
+        if not isinstance(topk_weights, torch.Tensor) or topk_weights.numel() < M * topk:
+            raise ValueError("chord_w4a16_moe_gemm: the weighted add needs topk_weights [M, topk]")
+        _check_operands(A, A, K, K, CHORD_EPI_STORE, cap, 0, "chord_w4a16_moe_gemm")
+    else:
+        _check_operands(A, C, K, N, epilogue, M if a_gather else cap, cap, "chord_w4a16_moe_gemm")
     tun = _tuning(tuning)
     _check(lib().chord_w4a16_moe_gemm(
         _ptr(A, None, "A"), int(a_gather), _ptr(packed_w, torch.uint8, "packed_w"), E_local, N, K, M,
@@ -245,7 +261,8 @@ def chord_w4a16_moe_gemm(A, a_gather: bool, packed_w, E_local: int, N: int, K: i
         _ptr(num_tokens_post_padded, torch.int32, "num_tokens_post_padded"),
         _ptr(expert_counts, torch.int32, "expert_counts"),
         _ptr(expert_offsets, torch.int32, "expert_offsets"), block_m, sorted_token_ids.numel(),
-        epilogue, _ptr(C, None, "C"), tun[0] if tun else None, _ptr(workspace, torch.uint8, "workspace"),
+        epilogue, _ptr(topk_weights, torch.float32, "topk_weights"), _ptr(C, None, "C"),
+        tun[0] if tun else None, _ptr(workspace, torch.uint8, "workspace"),
         workspace.numel(), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 

@@ -1,5 +1,6 @@
 // C ABI of the chord_moe library: argument checks, workspace carving, path
 // selection and launches.  No entry point allocates memory or synchronises.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -11,6 +12,9 @@
 namespace {
 
 thread_local char g_err[512] = "";
+// Test hook (chord_debug_force_timeout): later small-M GEMM launches
+// withhold their work items from the consumer warps.
+std::atomic<int> g_force_timeout{0};
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -149,7 +153,7 @@ size_t layer_ws_max(int M, int H, int I, int E_local, int topk) {
 int check_gemm_shapes(int N, int K, int epilogue) {
   if (K <= 0 || K % 64 != 0) return fail(CHORD_ERR_INVALID_ARG, "K=%d must be a positive multiple of 64", K);
   if (N <= 0 || N % 16 != 0) return fail(CHORD_ERR_INVALID_ARG, "N=%d must be a positive multiple of 16", N);
-  if (epilogue != CHORD_EPI_STORE && epilogue != CHORD_EPI_SILU_MUL)
+  if (epilogue != CHORD_EPI_STORE && epilogue != CHORD_EPI_SILU_MUL && epilogue != CHORD_EPI_WEIGHTED_ADD)
     return fail(CHORD_ERR_INVALID_ARG, "unknown epilogue %d", epilogue);
   if (epilogue == CHORD_EPI_SILU_MUL && N % 64 != 0)
     return fail(CHORD_ERR_INVALID_ARG, "SiLU*mul needs N=2I with I %% 32 == 0 (N=%d)", N);
@@ -161,6 +165,11 @@ int check_gemm_shapes(int N, int K, int epilogue) {
 extern "C" {
 
 const char* chord_last_error_string(void) { return g_err; }
+
+int chord_debug_force_timeout(int enable) {
+  g_force_timeout.store(enable ? 1 : 0, std::memory_order_relaxed);
+  return CHORD_OK;
+}
 
 int chord_version(void) { return 100; }
 
@@ -345,8 +354,8 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
                      int K, int M, int topk, const int32_t* sorted_token_ids,
                      const int32_t* expert_ids, const int32_t* ntpp, const int32_t* expert_counts,
                      const int32_t* expert_offsets, int block_m, size_t capacity, int epilogue,
-                     chord_bf16* C, const chord_tuning* tuning, double tok_e, const GemmWs& ws,
-                     int* dev_status, void* stream, int pdl = 0) {
+                     void* C, const chord_tuning* tuning, double tok_e, const GemmWs& ws,
+                     int* dev_status, void* stream, int pdl = 0, const float* topk_weights = nullptr) {
   int rc = check_tuning(tuning);
   if (rc) return rc;
   rc = check_gemm_shapes(N, K, epilogue);
@@ -359,6 +368,11 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
   if (!aligned16(A) || !aligned16(packed_w) || !aligned16(C))
     return fail(CHORD_ERR_INVALID_ARG, "A, packed_w and C must be 16-byte aligned");
   if (!ws.work) return fail(CHORD_ERR_WORKSPACE_TOO_SMALL, "no GEMM workspace");
+  if (epilogue == CHORD_EPI_WEIGHTED_ADD) {
+    if (a_gather) return fail(CHORD_ERR_UNSUPPORTED, "the weighted-add epilogue reads rows in sorted order (a_gather = 0)");
+    if (!topk_weights || !sorted_token_ids)
+      return fail(CHORD_ERR_INVALID_ARG, "the weighted-add epilogue needs topk_weights and sorted_token_ids");
+  }
   if (M == 0) return CHORD_OK;
   int path = tuning && tuning->path ? tuning->path : CHORD_PATH_AUTO;
   if (path == CHORD_PATH_AUTO)
@@ -383,8 +397,11 @@ static int gemm_impl(const chord_bf16* A, int a_gather, const void* packed_w, in
   g.work = ws.work;
   g.split_cnt = ws.split_cnt;
   g.split_partial = ws.split_partial;
+  g.test_timeout = g_force_timeout.load(std::memory_order_relaxed) ? 1 : 0;
   g.epilogue = epilogue;
-  g.C = C;
+  g.C = epilogue == CHORD_EPI_WEIGHTED_ADD ? nullptr : static_cast<uint16_t*>(C);
+  g.Cf = epilogue == CHORD_EPI_WEIGHTED_ADD ? static_cast<float*>(C) : nullptr;
+  g.topk_w = topk_weights;
   g.status = dev_status;
   g.pdl = pdl;
   const size_t max_blocks = (capacity + block_m - 1) / block_m;
@@ -424,6 +441,8 @@ int grouped_impl(const chord_bf16* A, size_t capacity, const int32_t* group_rows
   rc = check_gemm_shapes(N, K, epilogue);
   if (rc) return rc;
   if (E < 1 || E > 1024) return fail(CHORD_ERR_INVALID_ARG, "E=%d not in [1, 1024]", E);
+  if (epilogue == CHORD_EPI_WEIGHTED_ADD)
+    return fail(CHORD_ERR_INVALID_ARG, "the weighted-add epilogue needs routing (chord_w4a16_moe_gemm)");
   if (capacity > 0x7fffffffu) return fail(CHORD_ERR_INVALID_ARG, "%zu rows: too many", capacity);
   if (capacity == 0) return CHORD_OK;
   if (!A || !group_rows || !packed_w || !C) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
@@ -498,8 +517,9 @@ int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w
                          int N, int K, int M, int topk, const int32_t* sorted_token_ids,
                          const int32_t* expert_ids, const int32_t* num_tokens_post_padded,
                          const int32_t* expert_counts, const int32_t* expert_offsets, int block_m,
-                         size_t capacity, int epilogue, chord_bf16* C, const chord_tuning* tuning,
-                         void* workspace, size_t ws_bytes, int* dev_status, void* stream) {
+                         size_t capacity, int epilogue, const float* topk_weights, void* C,
+                         const chord_tuning* tuning, void* workspace, size_t ws_bytes, int* dev_status,
+                         void* stream) {
   const double tok_e = E_local > 0 ? static_cast<double>(M) * topk / E_local : 0.0;
   int rc = check_tuning(tuning);   // argument errors take precedence over the workspace size
   if (rc) return rc;
@@ -513,7 +533,7 @@ int chord_w4a16_moe_gemm(const chord_bf16* A, int a_gather, const void* packed_w
   gws.gather_bytes = ws_bytes - kWorkBytes - kSplitBytes;
   return gemm_impl(A, a_gather, packed_w, E_local, N, K, M, topk, sorted_token_ids, expert_ids,
                    num_tokens_post_padded, expert_counts, expert_offsets, block_m, capacity, epilogue,
-                   C, tuning, tok_e, gws, dev_status, stream);
+                   C, tuning, tok_e, gws, dev_status, stream, 0, topk_weights);
 }
 
 // [256 B work counters | counts, offsets, ntpp (256 B) | expert_ids |
@@ -531,6 +551,8 @@ int chord_w4a16_gemm(const chord_bf16* A, const void* packed_w, int N, int K, in
   rc = check_gemm_shapes(N, K, epilogue);
   if (rc) return rc;
   if (M < 0) return fail(CHORD_ERR_INVALID_ARG, "M=%d < 0", M);
+  if (epilogue == CHORD_EPI_WEIGHTED_ADD)
+    return fail(CHORD_ERR_INVALID_ARG, "the weighted-add epilogue needs routing (chord_w4a16_moe_gemm)");
   if (M == 0) return CHORD_OK;
   if (!A || !packed_w || !C) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
   if (!workspace || !aligned16(workspace)) return fail(CHORD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");

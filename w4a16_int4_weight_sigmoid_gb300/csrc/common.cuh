@@ -152,10 +152,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Poll limit: each try_wait may suspend the thread for a while, so this is
 // seconds of waiting, far beyond any legitimate stall.
 constexpr uint32_t kWaitPolls = 1u << 24;
+// Poll limit of the waits a test of the timeout path makes run out.
+constexpr uint32_t kTestWaitPolls = 1024;
 
-// Returns false (and records a timeout) if the phase did not complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
+// Returns false (and records a timeout) if the phase did not complete
+// within `polls` probes.  Waits for a CTA's own copies in flight before it
+// exits always use the full kWaitPolls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   set_status(status, CHORD_ERR_TIMEOUT);
   return false;
@@ -163,8 +168,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 
 // Same, for a thread that is not latency critical (a producer waiting for a
 // free slot): sleeps briefly between probes instead of spinning.
-__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, int* status) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, int* status,
+                                                  uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     __nanosleep(64);
   }

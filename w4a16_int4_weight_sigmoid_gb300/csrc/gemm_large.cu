@@ -90,6 +90,10 @@ struct LargeArgs {
   const int32_t* offsets;
   int* work;        // [0] next item, [1] CTAs done; zero before the launch, zero after it
   uint16_t* C;
+  float* Cf;             // weighted add: FP32 [M, N] accumulator (else NULL)
+  const float* topk_w;   // weighted add: routing weights [M, topk]
+  const int32_t* sorted; // weighted add: sorted_token_ids
+  int M, topk;
   int* status;
   int N, K, ldc, E_local, n_blob_tiles;
   int64_t tile_bytes;
@@ -506,6 +510,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               a.C[static_cast<size_t>(item.row0 + c0 + c) * a.ldc + col] = f32_to_bf16_rn(h);
             }
           }
+        } else if (a.Cf) {
+          // weighted add: lane c holds row c's assignment and weight; each
+          // column c of the accumulator goes, scaled, into that token's row
+          const int col = kMRows * item.wt + row_in;
+          int f = -1;
+          float w = 0.f;
+          if (lane < ncol) {
+            f = ld_cg(a.sorted + item.row0 + c0 + lane);
+            if (f < 0 || f >= a.M * a.topk) f = -1;
+            else w = ld_cg(a.topk_w + f);
+          }
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int fc = __shfl_sync(0xffffffffu, f, c);
+            const float wc = __shfl_sync(0xffffffffu, w, c);
+            if (c < ncol && fc >= 0)
+              atomicAdd(a.Cf + static_cast<size_t>(fc / a.topk) * a.N + col, wc * __uint_as_float(v[c]));
+          }
         } else {
           const int col = kMRows * item.wt + row_in;
 #pragma unroll
@@ -588,6 +610,11 @@ cudaError_t gemm_large_launch(const GemmLaunch& g, const uint16_t* B, size_t b_r
   a.offsets = g.offsets;
   a.work = g.work;
   a.C = g.C;
+  a.Cf = g.epilogue == CHORD_EPI_WEIGHTED_ADD ? g.Cf : nullptr;
+  a.topk_w = g.topk_w;
+  a.sorted = g.sorted;
+  a.M = g.M;
+  a.topk = g.topk;
   a.status = g.status;
   a.N = g.N;
   a.K = g.K;

@@ -32,8 +32,9 @@
 //     -136 * sum(x) by two extra MMAs on the busier tensor pipe, and was
 //     5-12 % slower;
 //   * epilogue: SiLU(gate) * up (a gate/up slab holds gate rows g and up rows
-//     g + 8 of the same intermediate index, so both land in one thread) or a
-//     plain store, BF16, rows in sorted order;
+//     g + 8 of the same intermediate index, so both land in one thread), a
+//     plain store, BF16, rows in sorted order, or the weighted add (FP32
+//     atomic adds of topk_weights[f] * acc into the token's row);
 //   * split-K, gated on grid saturation ([Chord] "인덱스 커널 기법": stream-K
 //     only where the grid is not already full): when a launch has at most
 //     half as many items as resident CTAs (a few decode tokens touching one
@@ -87,9 +88,13 @@ struct SmallArgs {
   int* work;        // [0] next item, [1] CTAs done; zero before the launch, zero after it
   int block_m;
   uint16_t* C;
+  float* Cf;             // weighted add: FP32 [M, N] accumulator
+  const float* topk_w;   // weighted add: routing weights [M, topk]
   int* status;
-  int N, K, topk, ldc, n_tiles, E_local;
+  int N, K, M, topk, ldc, n_tiles, E_local;
   int pdl, max_blocks;   // programmatic-launch mode (GemmLaunch::pdl); capacity / block_m
+  uint32_t wait_polls;   // probes per main-loop barrier wait (drains always use kWaitPolls)
+  int test_timeout;      // test hook: hand out no item, so the consumers' waits run out
   float* partial;        // split-K partial accumulators (kSplitSlots slots); NULL: no split-K
   int* split_cnt;        // per (item, consumer warp) arrival counters, zero between launches
   int64_t tile_bytes;
@@ -309,9 +314,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     const long long total = n_base * nsplit;
     if (a.pdl == 2) {
       int i = 0;
-      if (lane == 0) i = atomicAdd(a.work, 1);
+      if (lane == 0 && !a.test_timeout) i = atomicAdd(a.work, 1);
       i = __shfl_sync(0xffffffffu, i, 0);
-      first = decode_item(i, total, nblocks, nsplit, 2);
+      first = decode_item(a.test_timeout ? static_cast<int>(total) : i, total, nblocks, nsplit, 2);
       const int rows0 = min(Cfg::kRowsPerPass, first.rows);
       if (rows0 > 0) {
         pre = min(STAGES, first.ks1 - first.ks0);
@@ -322,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       for (int j = 0; j < pre; ++j) issue_rows(first, 0, rows0, first.ks0 + j, j);
     }
     int it = 0, q = 0;
-    bool ok = true, use_first = a.pdl == 2;
+    bool ok = !a.test_timeout, use_first = a.pdl == 2 && !a.test_timeout;   // test hook: no item at all
     while (ok) {
       SItem item;
       if (use_first) {   // fetched before the wait
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       }
       const int slot = q % kItemSlots;
       if (q >= kItemSlots)
-        ok = mbar_wait_backoff(&item_empty[slot], ((q / kItemSlots) - 1) & 1, a.status);
+        ok = mbar_wait_backoff(&item_empty[slot], ((q / kItemSlots) - 1) & 1, a.status, a.wait_polls);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       if (lane == 0) {
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
             continue;
           }
           const int s = it % STAGES;
-          if (it >= STAGES) ok = mbar_wait_backoff(&empty_bar[s], ((it / STAGES) - 1) & 1, a.status);
+          if (it >= STAGES) ok = mbar_wait_backoff(&empty_bar[s], ((it / STAGES) - 1) & 1, a.status, a.wait_polls);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
           issue_weights(wtile, item.ntl, rows, ks, s);
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
   int it = 0;
   for (int q = 0;; ++q) {
     const int slot = q % kItemSlots;
-    if (!mbar_wait(&item_full[slot], (q / kItemSlots) & 1, a.status)) return;
+    if (!mbar_wait(&item_full[slot], (q / kItemSlots) & 1, a.status, a.wait_polls)) return;
     const SItem item = item_q[slot];
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[slot]);
@@ -401,6 +406,18 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
         for (int i = 0; i < 2; ++i) {
           const int tok = n * 8 + 2 * t + i;
           if (tok >= rows) continue;
+          if (EPI == CHORD_EPI_WEIGHTED_ADD) {
+            // the row's assignment f: token f / topk, weight topk_w[f]
+            // (read from L2: written by earlier kernels); padding rows skip
+            const int f = ld_cg(a.sorted + r0 + tok);
+            if (f < 0 || f >= a.M * a.topk) continue;
+            const float w = ld_cg(a.topk_w + f);
+            float* crow = a.Cf + static_cast<size_t>(f / a.topk) * a.N;
+            const int col = kTileRows * tile + 16 * warp + g;
+            if (col < a.N) atomicAdd(crow + col, w * acc[n][i]);
+            if (col + 8 < a.N) atomicAdd(crow + col + 8, w * acc[n][2 + i]);
+            continue;
+          }
           uint16_t* crow = a.C + (r0 + tok) * a.ldc;
           if (EPI == CHORD_EPI_SILU_MUL) {
             // acc[n][i]: gate of index i0 + g; acc[n][2 + i]: up of the same index
@@ -419,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       for (int pass = 0; pass < passes; ++pass, ++it) {
         const int rows = min(Cfg::kRowsPerPass, item.rows - pass * Cfg::kRowsPerPass);
         const int s = it % STAGES;
-        if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status)) return;
+        if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status, a.wait_polls)) return;
         const uint32_t st = smem_base + s * Cfg::kStageBytes;
 #pragma unroll 1
         for (int tl = 0; tl < item.ntl; ++tl) {
@@ -448,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
 
       for (int ks = item.ks0; ks < item.ks1; ++ks, ++it) {
         const int s = it % STAGES;
-        if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status)) return;
+        if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status, a.wait_polls)) return;
         const uint32_t st = smem_base + s * Cfg::kStageBytes;
         const int units = min(kUnitsPerStage, n_units - ks * kUnitsPerStage);
         if (units == kUnitsPerStage) {
@@ -535,9 +552,11 @@ cudaError_t launch_small(const SmallArgs& a, cudaStream_t st) {
 template <int NT, int STAGES>
 cudaError_t dispatch_mode(const SmallArgs& a, bool gather, int epi, cudaStream_t st) {
   if (gather) {
+    if (epi == CHORD_EPI_WEIGHTED_ADD) return cudaErrorInvalidValue;   // refused by the host checks
     return epi == CHORD_EPI_SILU_MUL ? launch_small<NT, STAGES, true, CHORD_EPI_SILU_MUL>(a, st)
                                      : launch_small<NT, STAGES, true, CHORD_EPI_STORE>(a, st);
   }
+  if (epi == CHORD_EPI_WEIGHTED_ADD) return launch_small<NT, STAGES, false, CHORD_EPI_WEIGHTED_ADD>(a, st);
   return epi == CHORD_EPI_SILU_MUL ? launch_small<NT, STAGES, false, CHORD_EPI_SILU_MUL>(a, st)
                                    : launch_small<NT, STAGES, false, CHORD_EPI_STORE>(a, st);
 }
@@ -559,11 +578,16 @@ cudaError_t gemm_small_launch(const GemmLaunch& g, int rows_per_pass, cudaStream
   a.status = g.status;
   a.N = g.N;
   a.K = g.K;
+  a.M = g.M;
   a.topk = g.topk;
+  a.Cf = g.Cf;
+  a.topk_w = g.topk_w;
   a.E_local = g.E_local;
   a.pdl = g.pdl;
   a.max_blocks = g.max_blocks;
   a.partial = g.split_cnt ? g.split_partial : nullptr;
+  a.test_timeout = g.test_timeout;
+  a.wait_polls = g.test_timeout ? kTestWaitPolls : kWaitPolls;
   a.split_cnt = g.split_cnt;
   const PackHeader h = make_pack_header(g.E_local, g.N, g.K, g.epilogue == CHORD_EPI_SILU_MUL);
   a.n_tiles = h.n_tiles;

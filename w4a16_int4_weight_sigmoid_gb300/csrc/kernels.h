@@ -46,7 +46,9 @@ struct GemmLaunch {
   int block_m;
   int* work;        // small-M path: 2 ints, zero before the first launch (kept zero)
   int epilogue;
-  uint16_t* C;
+  uint16_t* C;             // BF16 output (STORE, SILU_MUL)
+  float* Cf = nullptr;     // FP32 [M, N] accumulator (WEIGHTED_ADD)
+  const float* topk_w = nullptr;   // routing weights [M, topk] (WEIGHTED_ADD)
   int* status;
   // Programmatic launch (small-M path only): 0 ordinary; 1 the kernel may
   // start before the previous kernel ends and waits for it before reading
@@ -60,6 +62,10 @@ struct GemmLaunch {
   // kernel never splits K.
   float* split_partial = nullptr;
   int* split_cnt = nullptr;
+  // Test of the timeout path (chord_debug_force_timeout): the small-M
+  // kernel's producer issues no copy and hands out no item, and the
+  // consumers give up their wait for an item after kTestWaitPolls probes.
+  int test_timeout = 0;
 };
 // Dense GEMM: one-expert block map (counts, offsets, ntpp, expert_ids) for M rows.
 cudaError_t dense_setup_launch(int M, int bm, int32_t* counts, int32_t* offsets, int32_t* ntpp,
