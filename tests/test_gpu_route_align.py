@@ -184,7 +184,8 @@ def check_route_align(logits, bias, k, begin, E_local, bm):
 @pytest.mark.parametrize("M", wl.ROUTER_ALIGN_M)
 @pytest.mark.parametrize("bm", wl.ROUTER_ALIGN_BM)
 def test_route_align_fused_router_workload(M, bm):
-    """One launch up to 16 tokens (M = 1, 8); larger M takes the two-launch path."""
+    """One launch up to 16 tokens (M = 1: one warp; M = 8: one CTA); larger M
+    takes the two-launch path."""
     logits, bias = wl.router_inputs(M, wl.ROUTER_ALIGN_E, wl.ROUTER_ALIGN_SEED)
     check_route_align(logits, bias, wl.ROUTER_ALIGN_TOPK, 0, wl.ROUTER_ALIGN_E, bm)
 
@@ -196,6 +197,13 @@ def test_route_align_fused_router_workload(M, bm):
     (7, 1, 1, 0, 1, 128),
     (9, 1000, 17, 500, 500, 64),
     (0, 384, 8, 0, 48, 16),
+    # up to 32 assignments: one warp routes and aligns
+    (32, 384, 1, 0, 384, 16),       # 32 tokens at top-1
+    (4, 384, 8, 100, 48, 128),      # 32 assignments, shard in the middle, long padding
+    (3, 64, 8, 0, 64, 8),
+    (2, 1024, 16, 0, 1024, 16),     # widest router
+    (1, 384, 8, 376, 8, 16),        # shard at the end
+    (2, 384, 8, 300, 3, 32),        # few local experts, most assignments dropped
 ])
 def test_route_align_fused_edges(M, E, k, begin, E_local, bm):
     logits, bias = wl.router_inputs(M, E, 41)

@@ -52,14 +52,19 @@ __device__ void chunk_rank(const AlignArgs& a, int g, int* s, int (&loc)[kPerThr
   for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
   __syncthreads();
   const uint32_t lt = (1u << lane) - 1u;
+  // All of this thread's ids are loaded before any is ranked, so the loads
+  // are in flight together (ordered L2 loads: the ids may come from the
+  // preceding kernel).
+  int eid[kPerThread];
 #pragma unroll
   for (int step = 0; step < kPerThread; ++step) {
     const int idx = elem_index(g, warp, step, lane);
-    int e = -1;
-    if (idx < a.n) {
-      e = ld_cg(a.ids + idx) - a.begin;   // ordered L2 load: ids may come from the preceding kernel
-      if (e < 0 || e >= E) e = -1;
-    }
+    eid[step] = idx < a.n ? ld_cg(a.ids + idx) : a.begin - 1;
+  }
+#pragma unroll
+  for (int step = 0; step < kPerThread; ++step) {
+    int e = eid[step] - a.begin;
+    if (e < 0 || e >= E) e = -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     const int leader = __ffs(peers) - 1;
     int base = 0;

@@ -1,4 +1,4 @@
-// Fused router + align for the smallest batches (up to 16 tokens): one CTA
+// Fused router + align for small batches (up to 16 tokens): one CTA
 // routes every token (one warp per token, the router's own code), then,
 // after a block barrier that
 // makes its topk_ids writes visible to all its threads, runs the one-chunk
@@ -40,6 +40,99 @@ __global__ void __launch_bounds__(kThreads) route_align_kernel(RouteIn r, AlignA
   scatter_chunk(a, 0, s, loc, rank, scan_scratch);
 }
 
+// The smallest batches (M * topk <= 32 assignments, e.g. one decode token at
+// top-8): one small CTA without the general align's per-warp tables.  Warp
+// t routes token t (ids kept in shared memory as well as written out); warp
+// 0 then holds assignment f in lane f: a stable rank per expert from
+// __match_any_sync, the present experts' order and offsets from a 32-entry
+// table; finally every thread fills counts and offsets for its experts by a
+// binary search in that table.  Outputs are those of the general kernels.
+constexpr int kTinyWarps = 4, kTinyMaxWarps = 8;
+template <int EPL>
+__global__ void __launch_bounds__(32 * kTinyMaxWarps) route_align_tiny_kernel(RouteIn r, AlignArgs a) {
+  __shared__ int s_id[32];                          // routed expert of assignment f
+  __shared__ int s_le[32], s_pad[32];               // per lane of warp 0: expert it leads (or INT_MAX), pad
+  __shared__ int t_e[32], t_end[32], t_cnt[32];     // present experts in id order
+  __shared__ int s_nlead;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int t = warp; t < r.M; t += nw) {
+    const int id = route_token<EPL>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
+    if (lane < r.topk) s_id[t * r.topk + lane] = id;
+  }
+  __syncthreads();
+  const int n = a.n, bm = a.bm, E = a.E;
+  if (warp == 0) {
+    int e = lane < n ? s_id[lane] - a.begin : -1;
+    if (e < 0 || e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int leader = __ffs(peers) - 1;
+    const bool lead = e >= 0 && lane == leader;
+    const int cnt = __popc(peers);
+    const int pad = lead ? (cnt + bm - 1) / bm * bm : 0;
+    s_le[lane] = lead ? e : 0x7fffffff;
+    s_pad[lane] = pad;
+    __syncwarp();
+    // order among the present experts and the padded rows below this one
+    int below = 0, off = 0;
+    if (lead) {
+#pragma unroll 8
+      for (int l = 0; l < 32; ++l) {
+        if (s_le[l] < e) {
+          ++below;
+          off += s_pad[l];
+        }
+      }
+      t_e[below] = e;
+      t_end[below] = off + pad;
+      t_cnt[below] = cnt;
+    }
+    const uint32_t leaders = __ballot_sync(0xffffffffu, lead);
+    int total = pad;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    off = __shfl_sync(0xffffffffu, off, leader);
+    if (lane < n) {
+      if (e >= 0) {
+        const int pos = off + rank;
+        a.sorted[pos] = lane;
+        if (a.positions) a.positions[lane] = pos;
+      } else if (a.positions) {
+        a.positions[lane] = -1;
+      }
+    }
+    if (lead) {
+      for (int p = off + cnt; p < off + pad; ++p) a.sorted[p] = a.sentinel;
+      for (int b = off / bm; b < (off + pad) / bm; ++b) a.expert_ids[b] = e;
+    }
+    if (lane == 0) {
+      s_nlead = __popc(leaders);
+      a.ntpp[0] = total;
+    }
+  }
+  __syncthreads();
+  // every expert x: count, and the padded rows of the present experts below x
+  const int nlead = s_nlead;
+  for (int x = threadIdx.x; x <= E; x += blockDim.x) {
+    int lo = 0, hi = nlead;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (t_e[mid] < x) lo = mid + 1; else hi = mid;
+    }
+    a.offsets[x] = lo == 0 ? 0 : t_end[lo - 1];
+    if (x < E) a.counts[x] = (lo < nlead && t_e[lo] == x) ? t_cnt[lo] : 0;
+  }
+}
+
+template <int EPL>
+cudaError_t launch_tiny(const RouteIn& r, const AlignArgs& a, cudaStream_t st) {
+  const int warps = r.M > kTinyWarps ? (r.M < kTinyMaxWarps ? r.M : kTinyMaxWarps) : kTinyWarps;
+  route_align_tiny_kernel<EPL><<<1, 32 * warps, 0, st>>>(r, a);
+  return cudaGetLastError();
+}
+
 template <int EPL>
 cudaError_t launch_fused(const RouteIn& r, const AlignArgs& a, cudaStream_t st) {
   const size_t smem = align_smem_bytes(a.E);
@@ -52,9 +145,10 @@ cudaError_t launch_fused(const RouteIn& r, const AlignArgs& a, cudaStream_t st) 
 }  // namespace
 
 // One CTA routes one token per warp: beyond kWarps tokens a warp would route
-// several in turn and the separate router grid is faster.
+// several in turn and the separate router grid is faster.  Up to 32
+// assignments the one-warp kernel takes any number of tokens.
 bool route_align_fits(int M, long long assignments, int E_local) {
-  return M <= kWarps && assignments <= kChunk && E_local >= 1 && E_local <= 1024;
+  return (M <= kWarps || assignments <= 32) && assignments <= kChunk && E_local >= 1 && E_local <= 1024;
 }
 
 cudaError_t route_align_launch(const float* logits, const float* bias, int M, int E_total, int topk,
@@ -80,6 +174,15 @@ cudaError_t route_align_launch(const float* logits, const float* bias, int M, in
   a.ws_rank = nullptr;
   a.ws_counts = nullptr;
   const int epl = (E_total + 31) / 32;
+  if (a.n <= 32) {
+    if (epl <= 1) return launch_tiny<1>(r, a, st);
+    if (epl <= 2) return launch_tiny<2>(r, a, st);
+    if (epl <= 4) return launch_tiny<4>(r, a, st);
+    if (epl <= 8) return launch_tiny<8>(r, a, st);
+    if (epl <= 12) return launch_tiny<12>(r, a, st);
+    if (epl <= 16) return launch_tiny<16>(r, a, st);
+    return launch_tiny<32>(r, a, st);
+  }
   if (epl <= 1) return launch_fused<1>(r, a, st);
   if (epl <= 2) return launch_fused<2>(r, a, st);
   if (epl <= 4) return launch_fused<4>(r, a, st);

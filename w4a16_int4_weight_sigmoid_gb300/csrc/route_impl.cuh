@@ -49,9 +49,10 @@ __device__ __forceinline__ uint64_t pack_key(float key, int id) {
 }
 
 // Route token t with the calling (whole, converged) warp: EPL experts per
-// lane (e = lane + 32 i); writes topk_ids / topk_weights row t.
+// lane (e = lane + 32 i); writes topk_ids / topk_weights row t and returns,
+// in lanes 0 .. topk-1, the id of that rank.
 template <int EPL>
-__device__ __forceinline__ void route_token(const float* __restrict__ logits, const float* __restrict__ bias,
+__device__ __forceinline__ int route_token(const float* __restrict__ logits, const float* __restrict__ bias,
                                             int t, int E, int topk, float* __restrict__ w_out,
                                             int32_t* __restrict__ id_out) {
   const int lane = threadIdx.x & 31;
@@ -108,6 +109,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, co
     id_out[o] = my_id;
     w_out[o] = __fdiv_rn(my_s, S);
   }
+  return my_id;
 }
 
 }  // namespace
