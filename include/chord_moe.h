@@ -341,7 +341,7 @@ int chord_w4a16_grouped_gemm_masked(const chord_bf16* A, const int32_t* group_ro
  *   out[t, :] = sum over j = 0..topk-1 with sorted_positions[t*topk+j] >= 0 of
  *               topk_weights[t, j] * y[sorted_positions[t*topk+j], :]
  * accumulated in FP32 in increasing j, rounded once to BF16.  A token with
- * no local assignment gets zeros.  Requires H % 8 == 0.
+ * no local assignment gets zeros.  Requires H % 8 == 0 and topk <= 32.
  */
 int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions,
                   int M, int topk, int H, chord_bf16* out, void* stream);

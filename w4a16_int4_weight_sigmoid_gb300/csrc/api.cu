@@ -590,7 +590,8 @@ namespace {
 // the down GEMM ends and waits for it).
 int moe_sum_impl(const chord_bf16* y, const float* topk_weights, const int32_t* sorted_positions, int M,
                  int topk, int H, chord_bf16* out, void* stream, bool pdl, int y_rows = 0x7fffffff) {
-  if (M < 0 || topk < 1 || H <= 0 || H % 8 != 0) return fail(CHORD_ERR_INVALID_ARG, "bad M/topk/H (H %% 8 == 0)");
+  if (M < 0 || topk < 1 || topk > 32 || H <= 0 || H % 8 != 0)
+    return fail(CHORD_ERR_INVALID_ARG, "bad M/topk/H (1 <= topk <= 32, H %% 8 == 0)");
   if (M > 0 && (!y || !topk_weights || !sorted_positions || !out)) return fail(CHORD_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(y) || !aligned16(out)) return fail(CHORD_ERR_INVALID_ARG, "y and out must be 16-byte aligned");
   cudaError_t e = chord::moe_sum_launch(y, topk_weights, sorted_positions, M, topk, H, out,

@@ -1,6 +1,15 @@
 // Top-k weighted sum of expert outputs back to tokens (moe_fused_mul_sum,
 // [HumPR] "왜 이게 좋은가" 3).  out[t] = sum_j w[t,j] * y[pos(t,j)], FP32 in
 // increasing j, one rounding to BF16; 16-byte vector loads and stores.
+//
+// A CTA covers one token and a run of its columns.  Warp 0 reads the
+// token's positions and weights once and lists its local slots in shared
+// memory; then every thread owns VPT 16-byte column vectors and loads the
+// rows of up to 16 / VPT local slots at once before adding them in slot
+// order, so the row loads of a token are in flight together.  With many
+// tokens (prefill) a CTA takes a whole row (VPT = 8 at H = 7168); with few
+// (decode) the host picks a smaller VPT so that there are several CTAs per
+// SM, and then more rows are in flight per thread.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -8,63 +17,100 @@ namespace chord {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kColsPerCta = kThreads * 8;
+constexpr int kVecInFlight = 16;   // 16-byte vectors a thread loads before adding
 
 // kOrdered: a programmatic launch; y, w and pos come from kernels that may
 // still be running when this grid starts, so they are read after the wait
 // with ordered L2 loads (see grid_dep_wait), not through the read-only cache.
 // A position at or past y_rows counts as no assignment, so a position map
 // that a failed earlier kernel left unwritten cannot send a load out of y.
-template <bool kOrdered>
+template <bool kOrdered, int VPT>
 __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* y, const float* w,
                                                            const int32_t* pos, int topk, int H, int y_rows,
                                                            uint16_t* __restrict__ out) {
+  constexpr int kRows = kVecInFlight / VPT > 1 ? kVecInFlight / VPT : 1;   // rows in flight
+  __shared__ int s_pos[32];
+  __shared__ float s_w[32];
+  __shared__ int s_nloc;
   grid_dep_wait();
   grid_dep_launch();
-  const int t = blockIdx.x;
-  const int c = blockIdx.y * kColsPerCta + threadIdx.x * 8;
-  if (c >= H) return;
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  // Slots in groups of 8: positions and weights first, then every row load of
-  // the group, so the loads overlap instead of forming a dependent chain.
-  for (int j0 = 0; j0 < topk; j0 += 8) {
-    int p[8];
-    float wj[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const bool in = j0 + j < topk;
-      const size_t o = static_cast<size_t>(t) * topk + (in ? j0 + j : 0);
-      p[j] = in ? (kOrdered ? ld_cg(pos + o) : __ldg(pos + o)) : -1;
-      if (p[j] >= y_rows) p[j] = -1;
-      wj[j] = in ? (kOrdered ? ld_cg(w + o) : __ldg(w + o)) : 0.f;
+  const int t = blockIdx.x, tid = threadIdx.x;
+  if (tid < 32) {
+    int p = -1;
+    float wj = 0.f;
+    if (tid < topk) {
+      const size_t o = static_cast<size_t>(t) * topk + tid;
+      p = kOrdered ? ld_cg(pos + o) : __ldg(pos + o);
+      if (p >= y_rows) p = -1;
+      wj = kOrdered ? ld_cg(w + o) : __ldg(w + o);
     }
-    uint4 v[8];
+    // local slots, compacted in increasing j
+    const uint32_t local = __ballot_sync(0xffffffffu, p >= 0);
+    if (p >= 0) {
+      const int k = __popc(local & ((1u << tid) - 1u));
+      s_pos[k] = p;
+      s_w[k] = wj;
+    }
+    if (tid == 0) s_nloc = __popc(local);
+  }
+  __syncthreads();
+  const int nloc = s_nloc;
+  const int v0 = blockIdx.y * kThreads * VPT;
+  const int nvec = H / 8;
+  float acc[VPT][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      v[j] = make_uint4(0, 0, 0, 0);
-      if (p[j] >= 0) {
-        const uint16_t* src = y + static_cast<size_t>(p[j]) * H + c;
-        v[j] = kOrdered ? ld_cg_v4(src) : __ldg(reinterpret_cast<const uint4*>(src));
+  for (int k = 0; k < VPT; ++k)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[k][i] = 0.f;
+  for (int j0 = 0; j0 < nloc; j0 += kRows) {
+    uint4 v[kRows][VPT];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int c = v0 + tid + k * kThreads;
+        v[r][k] = make_uint4(0, 0, 0, 0);
+        if (j0 + r < nloc && c < nvec) {
+          const uint16_t* src = y + static_cast<size_t>(s_pos[j0 + r]) * H + 8 * c;
+          v[r][k] = kOrdered ? ld_cg_v4(src) : __ldg(reinterpret_cast<const uint4*>(src));
+        }
       }
-    }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (p[j] < 0) continue;
-      const uint32_t vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    for (int r = 0; r < kRows; ++r) {
+      if (j0 + r >= nloc) break;
+      const float wj = s_w[j0 + r];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(wj[j], bf16lo_to_f32(vv[i]), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wj[j], bf16hi_to_f32(vv[i]), acc[2 * i + 1]);
+      for (int k = 0; k < VPT; ++k) {
+        const uint32_t vv[4] = {v[r][k].x, v[r][k].y, v[r][k].z, v[r][k].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[k][2 * i] = fmaf(wj, bf16lo_to_f32(vv[i]), acc[k][2 * i]);
+          acc[k][2 * i + 1] = fmaf(wj, bf16hi_to_f32(vv[i]), acc[k][2 * i + 1]);
+        }
       }
     }
   }
-  uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    o[i] = uint32_t(f32_to_bf16_rn(acc[2 * i])) | (uint32_t(f32_to_bf16_rn(acc[2 * i + 1])) << 16);
-  *reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int k = 0; k < VPT; ++k) {
+    const int c = v0 + tid + k * kThreads;
+    if (c >= nvec) continue;
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = uint32_t(f32_to_bf16_rn(acc[k][2 * i])) | (uint32_t(f32_to_bf16_rn(acc[k][2 * i + 1])) << 16);
+    *reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <int VPT>
+cudaError_t launch_sum(const uint16_t* y, const float* w, const int32_t* pos, int M, int topk, int H,
+                       uint16_t* out, cudaStream_t st, bool pdl, int y_rows) {
+  const dim3 grid(M, (H / 8 + kThreads * VPT - 1) / (kThreads * VPT));
+  if (pdl)
+    return launch_kernel(moe_sum_kernel<true, VPT>, grid, dim3(kThreads), 0, st, true, y, w, pos, topk, H, y_rows,
+                         out);
+  return launch_kernel(moe_sum_kernel<false, VPT>, grid, dim3(kThreads), 0, st, false, y, w, pos, topk, H, y_rows,
+                       out);
 }
 
 }  // namespace
@@ -72,10 +118,28 @@ __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* y, co
 cudaError_t moe_sum_launch(const uint16_t* y, const float* w, const int32_t* pos, int M, int topk,
                            int H, uint16_t* out, cudaStream_t st, bool pdl, int y_rows) {
   if (M == 0) return cudaSuccess;
-  dim3 grid(M, (H + kColsPerCta - 1) / kColsPerCta);
-  if (pdl)
-    return launch_kernel(moe_sum_kernel<true>, grid, dim3(kThreads), 0, st, true, y, w, pos, topk, H, y_rows, out);
-  return launch_kernel(moe_sum_kernel<false>, grid, dim3(kThreads), 0, st, false, y, w, pos, topk, H, y_rows, out);
+  if (topk > 32) return cudaErrorInvalidValue;
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!sms[dev]) {
+    err = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+  }
+  // vectors per thread: fewer (more CTAs per token) until there are about
+  // four CTAs per SM
+  const int nvec = H / 8;
+  auto ctas = [&](int v) { return static_cast<long long>(M) * ((nvec + kThreads * v - 1) / (kThreads * v)); };
+  int vpt = 8;
+  while (vpt > 1 && ctas(vpt) < 4LL * sms[dev]) vpt /= 2;
+  switch (vpt) {
+    case 8: return launch_sum<8>(y, w, pos, M, topk, H, out, st, pdl, y_rows);
+    case 4: return launch_sum<4>(y, w, pos, M, topk, H, out, st, pdl, y_rows);
+    case 2: return launch_sum<2>(y, w, pos, M, topk, H, out, st, pdl, y_rows);
+    default: return launch_sum<1>(y, w, pos, M, topk, H, out, st, pdl, y_rows);
+  }
 }
 
 }  // namespace chord
