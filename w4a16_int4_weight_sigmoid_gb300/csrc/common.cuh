@@ -166,6 +166,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   return false;
 }
 
+// Both barriers' phases complete (parity p0 of b0 and p1 of b1).  The two
+// probes are issued back to back and their results combined, so a warp that
+// waits for two phases which have usually completed already pays one probe
+// latency instead of two.
+__device__ __forceinline__ bool mbar_try_wait2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+      "and.pred p, p, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, int* status,
+                                           uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i)
+    if (mbar_try_wait2(b0, p0, b1, p1)) return true;
+  set_status(status, CHORD_ERR_TIMEOUT);
+  return false;
+}
+
 // Same, for a thread that is not latency critical (a producer waiting for a
 // free slot): sleeps briefly between probes instead of spinning.
 __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, int* status,

@@ -7,8 +7,8 @@
 //   * work item = (local expert, 128 weight rows, pass of up to 192 of the
 //     expert's rows), numbered expert by expert; warp 0 takes the next
 //     number from a global counter (items differ in rows, so a static deal
-//     leaves SMs idle) and passes it to the other roles through a small
-//     mbarrier ring; the CTAs running at one time cover a few experts, whose
+//     leaves SMs idle), decodes it and hands it to the other roles through
+//     a small mbarrier ring; the CTAs running at one time cover a few experts, whose
 //     activation rows stay in L2; the last CTA to run dry zeroes the counter;
 //   * the MMA is "swap AB": the 128 weight rows are M, the expert's rows
 //     (tokens) are N (a multiple of 16 up to 192), so an expert's rows are
@@ -32,7 +32,8 @@
 //     (barrier waits, shared-memory loads, decode, TMEM store and fences,
 //     ~1.3k cycles measured), longer than the stage's MMAs, so one group
 //     alone left the tensor pipe idle; two groups halve the gap (prefill
-//     gate/up 593 -> 536 us on GB300);
+//     gate/up 593 -> 536 us on GB300); the waits on two barriers probe both
+//     at once (one probe latency instead of two: 531 -> 511 us);
 //   * warp 1 (MMA): TMEM allocation; the converged warp waits and one
 //     elected lane issues the MMAs (M=128) into one of two accumulators and
 //     commits slot release and item completion to mbarriers;
@@ -187,13 +188,21 @@ __device__ __forceinline__ void dequant_two_slabs(const uint8_t* pst, const uint
 }
 
 // Next item from the CTA's item ring (consumer q of this role): the global
-// item number, -1 at the end of the work, -2 on a timeout.  All lanes of the
-// calling warp wait; lane 0 releases the slot.
+// item number, -1 at the end of the work, -2 on a timeout, and in *out (when
+// given) the item as the producer decoded it, read before the slot is
+// released.  All lanes of the calling warp wait; lane 0 releases the slot.
 __device__ __forceinline__ int take_item(uint64_t* item_full, uint64_t* item_empty, const volatile int* item_q,
-                                         int q, int* status) {
+                                         const volatile int (*item_f)[kItemSlots], int q, int* status,
+                                         Item* out) {
   const int slot = q % kItemSlots;
   if (!mbar_wait(&item_full[slot], (q / kItemSlots) & 1, status)) return -2;
   const int i = item_q[slot];
+  if (out) {
+    out->e = item_f[0][slot];
+    out->wt = item_f[1][slot];
+    out->row0 = item_f[2][slot];
+    out->rows = item_f[3][slot];
+  }
   __syncwarp(__activemask());
   if ((threadIdx.x & 31) == 0) mbar_arrive(&item_empty[slot]);
   return i;
@@ -215,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t tfull_bar[kAccBufs], tempty_bar[kAccBufs], done_bar;
   __shared__ __align__(8) uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   __shared__ volatile int item_q[kItemSlots];
+  __shared__ volatile int item_f[4][kItemSlots];   // the item's e, wt, row0, rows
   __shared__ uint32_t tmem_base_s;
   __shared__ int prefix[kMaxExperts + 1];
   __shared__ int hdr_ok;
@@ -293,10 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           abort_flag = 1;
           break;
         }
+        // the item is decoded once, here, and handed to the other roles with
+        // its number (their item_of lookups were global loads on the path
+        // from one item to the next)
+        Item item{0, 0, 0, 0};
+        if (i >= 0) item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
+        item_f[0][slot] = item.e;
+        item_f[1][slot] = item.wt;
+        item_f[2][slot] = item.row0;
+        item_f[3][slot] = item.rows;
         item_q[slot] = i;
-        mbar_arrive(&item_full[slot]);   // release: the item number is visible to the waiters
+        mbar_arrive(&item_full[slot]);   // release: the item is visible to the waiters
         if (i < 0) break;
-        const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
         const uint8_t* t0 = a.packed + kPackHeaderBytes +
                             (static_cast<size_t>(item.e) * a.n_blob_tiles + 2 * item.wt) *
                                 static_cast<size_t>(a.tile_bytes);
@@ -329,12 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;
       for (int q = 0; !abort_flag; ++q) {
-        const int i = take_item(item_full, item_empty, item_q, q, a.status);
+        Item item;
+        const int i = take_item(item_full, item_empty, item_q, item_f, q, a.status, &item);
         if (i < 0) {
           if (i == -2) abort_flag = 1;
           break;
         }
-        const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
         const int n_mma = (item.rows + 15) & ~15;
         const bool small = n_mma <= a.box_s;
         const CUtensorMap* map = small ? &map_s : &map_b;
@@ -366,13 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, j = 0;
       bool issued_any = false;
       for (; !abort_flag; ++j) {
-        int i = take_item(item_full, item_empty, item_q, j, a.status);
+        Item item;
+        int i = take_item(item_full, item_empty, item_q, item_f, j, a.status, &item);
         i = __shfl_sync(0xffffffffu, i, 0);   // warp-uniform before elect.sync
         if (i < 0) {
           if (i == -2) abort_flag = 1;
           break;
         }
-        const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
         const int acc = j % kAccBufs, use = j / kAccBufs;
         if (use >= 1 && !mbar_wait(&tempty_bar[acc], (use - 1) & 1, a.status)) {
           abort_flag = 1;
@@ -384,8 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
         for (int ks = 0; ks < n_stages; ++ks, ++it) {
           const int sa = it % kSA, sb = it % kSB;
-          if (!mbar_wait(&a_full[sa], (it / kSA) & 1, a.status) ||
-              !mbar_wait(&b_full[sb], (it / kSB) & 1, a.status)) {
+          if (!mbar_wait2(&a_full[sa], (it / kSA) & 1, &b_full[sb], (it / kSB) & 1, a.status)) {
             abort_flag = 1;
             break;
           }
@@ -438,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
     int it = 0;
     for (int q = 0; !abort_flag; ++q) {
-      int i = take_item(item_full, item_empty, item_q, q, a.status);
+      int i = take_item(item_full, item_empty, item_q, item_f, q, a.status, nullptr);
       i = __shfl_sync(0xffffffffu, i, 0);
       if (i < 0) {
         if (i == -2) abort_flag = 1;
@@ -447,8 +464,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ks < n_stages; ++ks, ++it) {
         if ((it % kGroups) != grp) continue;
         const int sp = it % kSP, sa = it % kSA;
-        bool ok = mbar_wait(&p_full[sp], (it / kSP) & 1, a.status) &&
-                  (it < kSA || mbar_wait(&a_empty[sa], ((it / kSA) - 1) & 1, a.status));
+        // the packed stage, and (after the first kSA stages) the A slot
+        // released by the MMAs of stage it - kSA
+        bool ok = it < kSA ? mbar_wait(&p_full[sp], (it / kSP) & 1, a.status)
+                           : mbar_wait2(&p_full[sp], (it / kSP) & 1, &a_empty[sa], ((it / kSA) - 1) & 1, a.status);
         ok = __all_sync(0xffffffffu, ok);   // warp-uniform: the .sync.aligned work below
         if (!ok) {
           abort_flag = 1;
@@ -476,13 +495,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qw = warp & 3;                 // TMEM lane quarter of this warp
     int j = 0;
     for (; !abort_flag; ++j) {
-      int i = take_item(item_full, item_empty, item_q, j, a.status);
+      Item item;
+      int i = take_item(item_full, item_empty, item_q, item_f, j, a.status, &item);
       i = __shfl_sync(0xffffffffu, i, 0);
       if (i < 0) {
         if (i == -2) abort_flag = 1;
         break;
       }
-      const Item item = item_of(i, prefix, a.counts, a.offsets, E, n_wt);
       const int acc = j % kAccBufs, use = j / kAccBufs;
       if (!mbar_wait_backoff(&tfull_bar[acc], use & 1, a.status)) {
         abort_flag = 1;
