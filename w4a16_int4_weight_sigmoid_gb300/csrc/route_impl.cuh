@@ -80,12 +80,14 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, con
     uint64_t best = cand[0];
 #pragma unroll
     for (int i = 1; i < EPL; ++i) best = cand[i] > best ? cand[i] : best;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-      best = o > best ? o : best;
-    }
-    const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+    // warp maximum of the 64-bit keys in two 32-bit reductions: the largest
+    // key word, then the largest id word among the lanes holding that key
+    // (the id word is never 0, so 0 stands for "not a holder")
+    const uint32_t hi = static_cast<uint32_t>(best >> 32);
+    const uint32_t top_hi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t top_lo =
+        __reduce_max_sync(0xffffffffu, hi == top_hi ? static_cast<uint32_t>(best) : 0u);
+    const int id = static_cast<int>(0xFFFFFFFFu - top_lo);
     const int owner = id & 31, slot = id >> 5;
     float s_mine = 0.f;
 #pragma unroll
