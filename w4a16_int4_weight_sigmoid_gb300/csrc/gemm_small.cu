@@ -328,16 +328,37 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     }
     int it = 0, q = 0;
     bool ok = !a.test_timeout, use_first = a.pdl == 2 && !a.test_timeout;   // test hook: no item at all
+    // Items of one K stage are short next to the round trips of the counter
+    // and the expert map, so they are taken two at a time: lane j decodes
+    // item base + j, and the loop hands them out in order (TP8 down GEMM
+    // 73.8 -> 72.2 us; four or eight at a time measured no better or worse).
+    const int batch = (k_stages + nsplit - 1) / nsplit <= 1 ? 2 : 1;
+    SItem held{0, 0, 0, -1, 1, 0, 0, 0, 0};
+    int held_k = 0, held_n = 0;
     while (ok) {
       SItem item;
       if (use_first) {   // fetched before the wait
         item = first;
         use_first = false;
       } else {
-        int i = 0;
-        if (lane == 0) i = atomicAdd(a.work, 1);
-        i = __shfl_sync(0xffffffffu, i, 0);
-        item = decode_item(i, total, nblocks, nsplit, how);
+        if (held_k == held_n) {
+          int i = 0;
+          if (lane == 0) i = atomicAdd(a.work, batch);
+          i = __shfl_sync(0xffffffffu, i, 0);
+          held = decode_item(lane < batch ? i + lane : static_cast<int>(total), total, nblocks, nsplit, how);
+          held_k = 0;
+          held_n = batch;
+        }
+        item.tile = __shfl_sync(0xffffffffu, held.tile, held_k);
+        item.e = __shfl_sync(0xffffffffu, held.e, held_k);
+        item.row0 = __shfl_sync(0xffffffffu, held.row0, held_k);
+        item.rows = __shfl_sync(0xffffffffu, held.rows, held_k);
+        item.ntl = __shfl_sync(0xffffffffu, held.ntl, held_k);
+        item.ks0 = __shfl_sync(0xffffffffu, held.ks0, held_k);
+        item.ks1 = __shfl_sync(0xffffffffu, held.ks1, held_k);
+        item.base = __shfl_sync(0xffffffffu, held.base, held_k);
+        item.split = __shfl_sync(0xffffffffu, held.split, held_k);
+        ++held_k;
       }
       const int slot = q % kItemSlots;
       if (q >= kItemSlots)
