@@ -138,8 +138,11 @@ def test_gemm_direct_rows_and_header_check(path):
 
 # (M, topk, H, E_total, local experts): one CTA per (token, column block),
 # and the streaming form taken from 4096 items on (1100 tokens x 4 column
-# blocks, the last one ragged: H = 3976)
-@pytest.mark.parametrize("M,k,H,E,local", [(37, 4, 1024, 12, (2, 7)), (1100, 6, 3976, 40, (3, 25))])
+# blocks, the last one ragged: H = 3976); with rows of 4096 < H <= 8192
+# and at least 16 tokens per SM, persistent CTAs that carry the next token's
+# slots ahead (3001 tokens, a ragged last pass over the grid, H = 7160)
+@pytest.mark.parametrize("M,k,H,E,local", [(37, 4, 1024, 12, (2, 7)), (1100, 6, 3976, 40, (3, 25)),
+                                           (3001, 8, 7160, 64, (8, 40))])
 def test_moe_sum_against_oracle(M, k, H, E, local):
     logits, bias = wl.router_inputs(M, E, 12)
     w, ids, _ = oracle.route(logits, bias, k)
