@@ -16,7 +16,10 @@ the region of K steps is bracketed by a barrier and torch.cuda.synchronize(),
 and the max over ranks is reported.  Kernel durations (for the roofline)
 come from a second CUDA-event-timed region of K steps that runs the same
 layer as four graph replays (route+align, gate/up, down, combine: the
-layer's C-ABI calls one by one) with events between them.
+layer's C-ABI calls one by one) with events between them.  Clocks:
+nvidia-smi polls every 200 ms from before the timed regions to after them,
+and the same step keeps replaying untimed around them (about a second in
+all), so the samples are taken under the timed load.
 
 The JSON line's headline (`value`, `roofline`, ...) is the selected workload
 (default EP8 decode); unless --only is given, `workloads` carries the same
@@ -321,6 +324,18 @@ def peak_for(peaks, region_s):
     return peaks["bf16_tflops_sustained"], "sustained"
 
 
+def soak(reps, seconds):
+    """Replay the replicas' layer graphs, untimed, for about `seconds`."""
+    import torch
+    end = time.perf_counter() + seconds
+    i = 0
+    while time.perf_counter() < end:
+        for _ in range(16):
+            reps[i % len(reps)].layer_graph.replay()
+            i += 1
+        torch.cuda.synchronize()
+
+
 def measure_workload(shape, steps, warmup, R, world, rank, local, seed_base, e2e_steps, sampler_uuid):
     """Time one layer workload: K layer-graph replays (the step), then the
     same K steps as the layer's C-ABI calls one by one for kernel durations,
@@ -349,7 +364,11 @@ def measure_workload(shape, steps, warmup, R, world, rank, local, seed_base, e2e
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.3)
+    t_sampled = time.perf_counter()
+    # nvidia-smi polls every 200 ms, longer than the timed region of a short
+    # run: the same step keeps the GPU under the same load before and after
+    # the timed regions, so that every sample is taken under load
+    soak(reps, 0.3)
     t0.record()
     for i in range(steps):
         reps[i % R].layer_graph.replay()
@@ -376,7 +395,11 @@ def measure_workload(shape, steps, warmup, R, world, rank, local, seed_base, e2e
     k1.record()
     torch.cuda.synchronize()
     barrier(world)
+    soak(reps, 1.0 - (time.perf_counter() - t_sampled))
     clocks = sampler.stop()
+    if clocks is not None:
+        clocks["window"] = ("the timed regions plus untimed replays of the same step before and after them, "
+                            f"{time.perf_counter() - t_sampled:.2f} s in all")
     staged_ms = allreduce_max(k0.elapsed_time(k1), world)
     names = ["route_align", "gate_up", "down", "combine"]
     per = {n: [] for n in names}
@@ -510,7 +533,7 @@ def run_ours(args, world, rank, local):
             uuid = "GPU-" + uuid
     except Exception:
         uuid = None
-    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, steps // 10)
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(10, min(steps, 200))
     head, host = measure_workload(shape, steps, warmup, R, world, rank, local, shape.seed, e2e_steps, uuid)
     line = {"metric": METRIC, "value": head.pop("value"), "unit": head.pop("unit"), "n_gpus": world,
             "steps": head.pop("steps"), "warmup": head.pop("warmup"), "ms_per_step": head.pop("ms_per_step"),
@@ -530,7 +553,7 @@ def run_ours(args, world, rank, local):
             o_decode = other.M * other.topk / other.E_total < 64
             o_R = 2 if o_decode else 1
             o_steps = max(steps, 20)
-            o_e2e = max(3, o_steps // 10)
+            o_e2e = max(10, min(o_steps, 50))
             fields, h = measure_workload(other, o_steps, warmup, o_R, world, rank, local, other.seed, o_e2e, uuid)
             del h
             fields["tokens_per_s"] = fields.pop("value")
@@ -548,22 +571,26 @@ def oracle_tokens_per_s(shape, host, budget_s, max_tokens=None):
     w, ids, _ = oracle.route(host["logits"], host["bias"], shape.topk)
     local = np.any((ids >= shape.expert_begin) & (ids < shape.expert_begin + shape.E_local), axis=1)
     cand = np.nonzero(local)[0]
-    n, t_total, done = 0, 0.0, []
+    n, t_total, cpu_total, done = 0, 0.0, 0.0, []
     for tok in cand:
         t = time.perf_counter()
+        c = time.process_time()
         oracle.moe_layer_tokens(np.array([tok]), host["x"], host["logits"], host["bias"], host["w13_q"],
                                 host["w13_s"], host["w2_q"], host["w2_s"], shape.topk, shape.expert_begin)
+        cpu_total += time.process_time() - c
         t_total += time.perf_counter() - t
         n += 1
         done.append(int(tok))
         if t_total >= budget_s or (max_tokens and n >= max_tokens):
             break
-    return n / t_total, n, t_total
+    # threads the oracle kept busy on average: process CPU time over wall time
+    return n / t_total, n, t_total, cpu_total / t_total
 
 
 def cpu_baseline(shape, host, budget_s):
-    v, n, t = oracle_tokens_per_s(shape, host, budget_s)
-    return {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+    v, n, t, cores = oracle_tokens_per_s(shape, host, budget_s)
+    return {"value": v, "unit": "tokens/s", "cores": round(cores, 1), "cores_available": os.cpu_count(),
+            "kind": "oracle",
             "sample": f"{n} tokens (each with >= 1 local expert) of {shape.name}, one at a time "
                       f"through the FP64 numpy oracle, {t:.1f} s"}
 
@@ -579,13 +606,14 @@ def run_reference(args, world, rank):
     # each step is one token; stop early when the time budget runs out
     budget = 150.0
     oracle_tokens_per_s(shape, host, 1e9, max_tokens=max(1, min(warmup, 2)))
-    v, n, t = oracle_tokens_per_s(shape, host, budget, max_tokens=steps)
+    v, n, t, cores = oracle_tokens_per_s(shape, host, budget, max_tokens=steps)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
             "steps": n, "warmup": warmup, "ms_per_step": 1e3 * t / n, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": shape.name, "M": shape.M, "H": shape.H, "I": shape.I,
                        "E_total": shape.E_total, "E_local": shape.E_local, "topk": shape.topk},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": round(cores, 1),
+                             "cores_available": os.cpu_count(), "kind": "oracle",
                              "sample": f"{n} tokens of {shape.name} (one per step), FP64 numpy oracle"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
