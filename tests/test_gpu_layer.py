@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import oracle
+from w4a16_int4_weight_sigmoid_gb300 import chord
 from w4a16_int4_weight_sigmoid_gb300 import workload as wl
 from w4a16_int4_weight_sigmoid_gb300.layer import W4A16MoELayer
 
@@ -52,8 +53,10 @@ def test_layer_fresh_workspace_every_call():
     """The register-MMA path chains its kernels with programmatic launches:
     each kernel must read the previous kernel's outputs only after waiting
     for it.  A fresh workspace per call, filled with a pattern that cannot
-    be a valid block map (0x7F bytes) or with zeros, exposes any read that
-    comes too early, as a device status or as a wrong output."""
+    be a valid block map (0x7F bytes, 0xFF bytes: counters of 2^31 - 1 - ...
+    and -1) or with zeros, exposes any read that comes too early, as a device
+    status or as a wrong output; the work-queue counters in it are cleared by
+    the router kernel, on both GEMM paths."""
     shape = small("tp_zipf_fresh_ws", 48, 256, 192, 32, 32, 0, 6, 22, zipf=1.1)
     d = wl.layer_inputs(shape)
     ref, _, _ = oracle.moe_layer(d["x"], d["logits"], d["bias"], d["w13_q"], d["w13_s"],
@@ -62,14 +65,14 @@ def test_layer_fresh_workspace_every_call():
                           shape.expert_begin, shape.topk)
     x, lg, b = to_device(d["x"]), to_device(d["logits"]), to_device(d["bias"])
     n = layer.workspace(shape.M).numel()
-    first = None
-    for i in range(40):
-        layer._ws = torch.full((n,), 0x7F if i % 2 else 0, dtype=torch.uint8, device="cuda")
-        out = layer.forward(x, lg, b)
+    large = chord.chord_tuning(chord.CHORD_PATH_LARGE_M, 0, 0, 0)
+    for i in range(48):
+        layer._ws = torch.full((n,), (0, 0x7F, 0xFF)[i % 3], dtype=torch.uint8, device="cuda")
+        out = layer.forward(x, lg, b, tuning=large if i >= 24 else None)
         torch.cuda.synchronize()
         assert layer.dev_status.item() == 0, f"call {i}: device status {layer.dev_status.item()}"
         got = bf16_to_np(out)
-        if first is None:
+        if i in (0, 24):   # each path against the oracle, then against itself
             assert_close_to_oracle(got, ref, shape.name)
             first = got
         else:

@@ -128,7 +128,7 @@ LayerWs layer_ws(int M, int H, int I, int E_local, int topk, int bm) {
   w.pos = take(mk * sizeof(int32_t));
   w.align_ws = take(chord::align_workspace_bytes(static_cast<long long>(mk), E_local));
   w.h = take(w.cap * static_cast<size_t>(I) * 2);
-  // Counters, zeroed by one memset per call: [down work | gate/up work |
+  // Counters, cleared by the router kernel on every call: [down work | gate/up work |
   // down split-K | gate/up split-K]; then the split-K partials, shared by
   // the two GEMMs (the down GEMM writes them only after the gate/up GEMM
   // has completed); then y, whose region holds the gathered x rows of the
@@ -234,7 +234,8 @@ int route_align_impl(const float* logits, const float* bias, int M, int E_total,
                      int expert_begin, int E_local, int block_m, size_t capacity, float* topk_weights,
                      int32_t* topk_ids, int32_t* sorted_token_ids, int32_t* expert_ids,
                      int32_t* num_tokens_post_padded, int32_t* expert_counts, int32_t* expert_offsets,
-                     int32_t* sorted_positions, void* workspace, size_t ws_bytes, void* stream, bool pdl);
+                     int32_t* sorted_positions, void* workspace, size_t ws_bytes, void* stream, bool pdl,
+                     int* zero = nullptr, int n_zero = 0);
 
 }  // namespace
 
@@ -270,7 +271,8 @@ int route_align_impl(const float* logits, const float* bias, int M, int E_total,
                      int expert_begin, int E_local, int block_m, size_t capacity, float* topk_weights,
                      int32_t* topk_ids, int32_t* sorted_token_ids, int32_t* expert_ids,
                      int32_t* num_tokens_post_padded, int32_t* expert_counts, int32_t* expert_offsets,
-                     int32_t* sorted_positions, void* workspace, size_t ws_bytes, void* stream, bool pdl) {
+                     int32_t* sorted_positions, void* workspace, size_t ws_bytes, void* stream, bool pdl,
+                     int* zero, int n_zero) {
   if (M < 0) return fail(CHORD_ERR_INVALID_ARG, "M=%d < 0", M);
   if (E_total < 1 || E_total > 1024) return fail(CHORD_ERR_INVALID_ARG, "E_total=%d not in [1, 1024]", E_total);
   if (topk < 1 || topk > E_total || topk > 32)
@@ -288,8 +290,9 @@ int route_align_impl(const float* logits, const float* bias, int M, int E_total,
   const long long n = static_cast<long long>(M) * topk;
   if (!chord::route_align_fits(M, n, E_local)) {
     // more than one chunk: the two separate launches
-    int rc = chord_moe_route(logits, bias, M, E_total, topk, topk_weights, topk_ids, stream);
-    if (rc) return rc;
+    cudaError_t er = chord::route_launch(logits, bias, M, E_total, topk, topk_weights, topk_ids,
+                                         static_cast<cudaStream_t>(stream), zero, n_zero);
+    if (er != cudaSuccess) return cuda_fail(er, "route launch");
     return align_impl(topk_ids, M, topk, expert_begin, E_local, block_m, capacity, sorted_token_ids,
                       expert_ids, num_tokens_post_padded, expert_counts, expert_offsets, sorted_positions,
                       workspace, ws_bytes, stream, pdl);
@@ -297,7 +300,7 @@ int route_align_impl(const float* logits, const float* bias, int M, int E_total,
   cudaError_t e = chord::route_align_launch(logits, bias, M, E_total, topk, expert_begin, E_local, block_m,
                                             topk_weights, topk_ids, sorted_token_ids, expert_ids,
                                             num_tokens_post_padded, expert_counts, expert_offsets,
-                                            sorted_positions, static_cast<cudaStream_t>(stream));
+                                            sorted_positions, static_cast<cudaStream_t>(stream), zero, n_zero);
   return e == cudaSuccess ? CHORD_OK : cuda_fail(e, "route+align launch");
 }
 
@@ -664,19 +667,22 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
   void* aws = ws + w.align_ws;
   chord_bf16* h = reinterpret_cast<chord_bf16*>(ws + w.h);
   chord_bf16* y = reinterpret_cast<chord_bf16*>(ws + w.y);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  cudaError_t ce = cudaMemsetAsync(ws + w.work, 0, 2 * kWorkBytes + 2 * kSplitCnt, st);
-  if (ce != cudaSuccess) return cuda_fail(ce, "work counter reset");
   // Register-MMA path: every kernel after the router is a programmatic
   // launch, so its launch and prologue overlap the end of the kernel before
   // it, and the down GEMM streams its first weight stages while the gate/up
   // GEMM finishes.  The tcgen05 path launches in plain stream order.
   const bool pdl = plan.path != CHORD_PATH_LARGE_M;
   // one launch when the assignments fit one align chunk, else two
+  // The router kernel (the layer's first) clears both GEMMs' work-queue and
+  // split counters; the GEMMs start after it has completed (stream order, or
+  // the launch chain: each kernel waits for the one before it, which waited
+  // for the router), so they always find them zero, also after a call that
+  // stopped on a timeout.
   rc = route_align_impl(logits, bias, M, E_total, topk, expert_begin, E_local, w.bm, w.cap, tw, ids, sorted,
                         eids, ntpp, counts, offsets, pos, aws, chord_moe_align_workspace_bytes(M, topk, E_local),
-                        stream, pdl);
+                        stream, pdl, reinterpret_cast<int*>(ws + w.work),
+                        static_cast<int>((2 * kWorkBytes + 2 * kSplitCnt) / sizeof(int)));
   if (rc) return rc;
   const double tok_e = static_cast<double>(M) * topk / E_total;
   GemmWs ws_gu, ws_dn;

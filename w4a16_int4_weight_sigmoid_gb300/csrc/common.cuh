@@ -203,6 +203,14 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Zero n ints at p (p may be NULL) with the whole grid: a layer's first
+// kernel clears the counters its later kernels use (they start after it has
+// completed, through the launch chain), instead of a separate memset.
+__device__ __forceinline__ void zero_ints(int* p, int n) {
+  if (!p) return;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
+}
+
 // ------------------------------------------------------- bulk async copies
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src 16-byte aligned, bytes a multiple of 16.

@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       for (int q = 0;; ++q) {
         int i = atomicAdd(a.work, 1);
-        if (i >= total_items || abort_flag) i = -1;
+        if (i < 0 || i >= total_items || abort_flag) i = -1;   // below zero: counters never zeroed
         const int slot = q % kItemSlots;
         if (q >= kItemSlots && !mbar_wait_backoff(&item_empty[slot], ((q / kItemSlots) - 1) & 1, a.status)) {
           abort_flag = 1;

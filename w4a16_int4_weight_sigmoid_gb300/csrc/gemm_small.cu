@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     // item i -> split s of base item i / S = (tile, block), block index fastest
     auto decode_item = [&](int i, long long total, int nblocks, int nsplit, int how) {
       SItem item{0, 0, 0, -1, 1, 0, 0, 0, 0};
-      if (i < total) {
+      if (i >= 0 && i < total) {   // below zero: counters never zeroed; no item
         const int base = i / nsplit, sp = i - base * nsplit;
         const int ng = base / nblocks, b = base - ng * nblocks;
         const int e = ld_map(a.expert_ids + b, how);

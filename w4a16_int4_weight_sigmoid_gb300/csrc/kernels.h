@@ -9,8 +9,9 @@ namespace chord {
 
 struct PackHeader;
 
+// zero, n_zero: ints the kernel clears (for the kernels after it; may be NULL)
 cudaError_t route_launch(const float* logits, const float* bias, int M, int E, int topk, float* w,
-                         int32_t* ids, cudaStream_t st);
+                         int32_t* ids, cudaStream_t st, int* zero = nullptr, int n_zero = 0);
 
 int align_num_chunks(long long n);
 size_t align_workspace_bytes(long long n, int E_local);
@@ -19,7 +20,7 @@ bool route_align_fits(int M, long long assignments, int E_local);
 cudaError_t route_align_launch(const float* logits, const float* bias, int M, int E_total, int topk,
                                int begin, int E_local, int bm, float* w, int32_t* ids, int32_t* sorted,
                                int32_t* expert_ids, int32_t* ntpp, int32_t* counts, int32_t* offsets,
-                               int32_t* positions, cudaStream_t st);
+                               int32_t* positions, cudaStream_t st, int* zero = nullptr, int n_zero = 0);
 cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_local, int bm,
                          int32_t* sorted, int32_t* expert_ids, int32_t* ntpp, int32_t* counts,
                          int32_t* offsets, int32_t* positions, void* ws, cudaStream_t st,

@@ -21,6 +21,8 @@ struct RouteIn {
   int M, E, topk;
   float* w;
   int32_t* ids;
+  int* zero;     // ints to clear for the kernels after this one (or NULL)
+  int n_zero;
 };
 
 template <int EPL>
@@ -30,6 +32,7 @@ __global__ void __launch_bounds__(kThreads) route_align_kernel(RouteIn r, AlignA
   const int warp = threadIdx.x >> 5;
   grid_dep_wait();
   grid_dep_launch();
+  zero_ints(r.zero, r.n_zero);
   for (int t = warp; t < r.M; t += kWarps) route_token<EPL>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
   __syncthreads();   // this CTA's topk_ids stores are visible to all its threads
   int loc[kPerThread], rank[kPerThread];
@@ -57,6 +60,7 @@ __global__ void __launch_bounds__(32 * kTinyMaxWarps) route_align_tiny_kernel(Ro
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   grid_dep_wait();
   grid_dep_launch();
+  zero_ints(r.zero, r.n_zero);
   for (int t = warp; t < r.M; t += nw) {
     const int id = route_token<EPL>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
     if (lane < r.topk) s_id[t * r.topk + lane] = id;
@@ -154,9 +158,9 @@ bool route_align_fits(int M, long long assignments, int E_local) {
 cudaError_t route_align_launch(const float* logits, const float* bias, int M, int E_total, int topk,
                                int begin, int E_local, int bm, float* w, int32_t* ids, int32_t* sorted,
                                int32_t* expert_ids, int32_t* ntpp, int32_t* counts, int32_t* offsets,
-                               int32_t* positions, cudaStream_t st) {
+                               int32_t* positions, cudaStream_t st, int* zero, int n_zero) {
   if (!route_align_fits(M, static_cast<long long>(M) * topk, E_local)) return cudaErrorInvalidValue;
-  RouteIn r{logits, bias, M, E_total, topk, w, ids};
+  RouteIn r{logits, bias, M, E_total, topk, w, ids, zero, n_zero};
   AlignArgs a;
   a.ids = ids;
   a.n = M * topk;
