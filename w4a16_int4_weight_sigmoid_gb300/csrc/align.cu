@@ -12,17 +12,18 @@
 namespace chord {
 namespace {
 
+template <int PER>
 __global__ void __launch_bounds__(kThreads) align_single_kernel(AlignArgs a) {
   extern __shared__ int s[];
   __shared__ int scan_scratch[kWarps + 1];
-  int loc[kPerThread], rank[kPerThread];
+  int loc[PER], rank[PER];
   grid_dep_wait();     // topk_ids come from the router kernel
   grid_dep_launch();
-  chunk_rank(a, 0, s, loc, rank);
+  chunk_rank<PER>(a, 0, s, loc, rank);
   int* base = sm_base(s, a.E);
   for (int e = threadIdx.x; e < a.E; e += kThreads) base[e] = 0;
   __syncthreads();
-  scatter_chunk(a, 0, s, loc, rank, scan_scratch);
+  scatter_chunk<PER>(a, 0, s, loc, rank, scan_scratch);
 }
 
 __global__ void __launch_bounds__(kThreads) align_rank_kernel(AlignArgs a) {
@@ -111,11 +112,19 @@ cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_l
   a.ws_counts = a.ws_rank ? a.ws_rank + a.n : nullptr;
   const size_t smem = align_smem_bytes(E_local);
   const int max_smem = static_cast<int>(align_smem_bytes(1024));
-  cudaError_t err = ensure_smem_limit<align_single_kernel>(max_smem);
+  cudaError_t err = ensure_smem_limit<align_single_kernel<1>>(max_smem);
+  if (err == cudaSuccess) err = ensure_smem_limit<align_single_kernel<2>>(max_smem);
+  if (err == cudaSuccess) err = ensure_smem_limit<align_single_kernel<kPerThread>>(max_smem);
   if (err == cudaSuccess) err = ensure_smem_limit<align_rank_kernel>(max_smem);
   if (err == cudaSuccess) err = ensure_smem_limit<align_scatter_kernel>(max_smem);
   if (err != cudaSuccess) return err;
-  if (a.G == 1) return launch_kernel(align_single_kernel, dim3(1), dim3(kThreads), smem, st, pdl, a);
+  if (a.G == 1) {
+    switch (align_per_thread(a.n)) {
+      case 1: return launch_kernel(align_single_kernel<1>, dim3(1), dim3(kThreads), smem, st, pdl, a);
+      case 2: return launch_kernel(align_single_kernel<2>, dim3(1), dim3(kThreads), smem, st, pdl, a);
+      default: return launch_kernel(align_single_kernel<kPerThread>, dim3(1), dim3(kThreads), smem, st, pdl, a);
+    }
+  }
   err = launch_kernel(align_rank_kernel, dim3(a.G), dim3(kThreads), smem, st, pdl, a);
   if (err != cudaSuccess) return err;
   align_scatter_kernel<<<a.G, kThreads, smem, st>>>(a);

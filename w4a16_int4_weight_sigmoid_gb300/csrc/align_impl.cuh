@@ -7,7 +7,10 @@
 // scatter cursors are re-initialised on entry as in "커널 내부 로직 변경").
 //
 // Each CTA owns a chunk of 4096 consecutive assignments; each of its 16
-// warps owns 256 consecutive ones, walked in 8 steps of 32.  Within a step,
+// warps owns 256 consecutive ones, walked in 8 steps of 32 (PER = 8).  A
+// one-chunk align of at most 512 or 1024 assignments spreads them over all
+// 16 warps instead (PER = 1 or 2: 32 or 64 per warp), so each warp walks one
+// or two steps.  Within a step,
 // __match_any_sync groups lanes with the same expert, the lowest lane of the
 // group advances the warp's counter for that expert, and each lane's rank is
 // the counter's old value plus the number of earlier lanes in its group.  An
@@ -39,13 +42,19 @@ __device__ __forceinline__ int* sm_tot(int* s, int E) { return s + kWarps * E; }
 __device__ __forceinline__ int* sm_base(int* s, int E) { return s + (kWarps + 1) * E; }
 __device__ __forceinline__ int* sm_off(int* s, int E) { return s + (kWarps + 2) * E; }
 
+template <int PER = kPerThread>
 __device__ __forceinline__ int elem_index(int g, int warp, int step, int lane) {
-  return g * kChunk + warp * (32 * kPerThread) + step * 32 + lane;
+  return g * kChunk + warp * (32 * PER) + step * 32 + lane;
+}
+
+// Elements per thread of a one-chunk align of n assignments.
+__host__ __device__ constexpr int align_per_thread(long long n) {
+  return n <= kThreads ? 1 : (n <= 2 * kThreads ? 2 : kPerThread);
 }
 
 // Per-chunk stable ranks; loc[] = local expert or -1; tot[e] = chunk count.
-__device__ void chunk_rank(const AlignArgs& a, int g, int* s, int (&loc)[kPerThread],
-                           int (&rank)[kPerThread]) {
+template <int PER = kPerThread>
+__device__ void chunk_rank(const AlignArgs& a, int g, int* s, int (&loc)[PER], int (&rank)[PER]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E;
   int* wcnt = sm_wcnt(s);
@@ -55,14 +64,14 @@ __device__ void chunk_rank(const AlignArgs& a, int g, int* s, int (&loc)[kPerThr
   // All of this thread's ids are loaded before any is ranked, so the loads
   // are in flight together (ordered L2 loads: the ids may come from the
   // preceding kernel).
-  int eid[kPerThread];
+  int eid[PER];
 #pragma unroll
-  for (int step = 0; step < kPerThread; ++step) {
-    const int idx = elem_index(g, warp, step, lane);
+  for (int step = 0; step < PER; ++step) {
+    const int idx = elem_index<PER>(g, warp, step, lane);
     eid[step] = idx < a.n ? ld_cg(a.ids + idx) : a.begin - 1;
   }
 #pragma unroll
-  for (int step = 0; step < kPerThread; ++step) {
+  for (int step = 0; step < PER; ++step) {
     int e = eid[step] - a.begin;
     if (e < 0 || e >= E) e = -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
@@ -78,18 +87,34 @@ __device__ void chunk_rank(const AlignArgs& a, int g, int* s, int (&loc)[kPerThr
   }
   __syncthreads();
   int* tot = sm_tot(s, E);
-  for (int e = tid; e < E; e += kThreads) {
-    int run = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      const int c = wcnt[w * E + e];
-      wcnt[w * E + e] = run;
-      run += c;
+  if (E <= 4 * kWarps) {
+    // few experts: one warp per expert column, the 16 warp counts scanned
+    // across lanes (five shuffles) instead of a 16-step loop per thread
+    for (int e = warp; e < E; e += kWarps) {
+      const int c = lane < kWarps ? wcnt[lane * E + e] : 0;
+      int inc = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      if (lane < kWarps) wcnt[lane * E + e] = inc - c;
+      if (lane == 31) tot[e] = inc;
     }
-    tot[e] = run;
+  } else {
+    for (int e = tid; e < E; e += kThreads) {
+      int run = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        const int c = wcnt[w * E + e];
+        wcnt[w * E + e] = run;
+        run += c;
+      }
+      tot[e] = run;
+    }
   }
   __syncthreads();
 #pragma unroll
-  for (int step = 0; step < kPerThread; ++step)
+  for (int step = 0; step < PER; ++step)
     if (loc[step] >= 0) rank[step] += wcnt[warp * E + loc[step]];
 }
 
@@ -127,8 +152,9 @@ __device__ void block_exclusive_scan(const int* in, int* out, int n, int* scratc
 
 // Given tot (all-chunk counts) and base (this chunk's start per expert):
 // offsets, scatter, metadata.
-__device__ void scatter_chunk(const AlignArgs& a, int g, int* s, const int (&loc)[kPerThread],
-                              const int (&rank)[kPerThread], int* scan_scratch) {
+template <int PER = kPerThread>
+__device__ void scatter_chunk(const AlignArgs& a, int g, int* s, const int (&loc)[PER],
+                              const int (&rank)[PER], int* scan_scratch) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, bm = a.bm;
   int* tot = sm_tot(s, E);
@@ -140,8 +166,8 @@ __device__ void scatter_chunk(const AlignArgs& a, int g, int* s, const int (&loc
   __syncthreads();
   block_exclusive_scan(pad, off, E, scan_scratch);
 #pragma unroll
-  for (int step = 0; step < kPerThread; ++step) {
-    const int idx = elem_index(g, warp, step, lane);
+  for (int step = 0; step < PER; ++step) {
+    const int idx = elem_index<PER>(g, warp, step, lane);
     if (idx >= a.n) continue;
     const int e = loc[step];
     if (e >= 0) {

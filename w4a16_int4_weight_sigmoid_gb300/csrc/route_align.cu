@@ -25,7 +25,7 @@ struct RouteIn {
   int n_zero;
 };
 
-template <int EPL>
+template <int EPL, int PER>
 __global__ void __launch_bounds__(kThreads) route_align_kernel(RouteIn r, AlignArgs a) {
   extern __shared__ int s[];
   __shared__ int scan_scratch[kWarps + 1];
@@ -35,12 +35,12 @@ __global__ void __launch_bounds__(kThreads) route_align_kernel(RouteIn r, AlignA
   zero_ints(r.zero, r.n_zero);
   for (int t = warp; t < r.M; t += kWarps) route_token<EPL>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
   __syncthreads();   // this CTA's topk_ids stores are visible to all its threads
-  int loc[kPerThread], rank[kPerThread];
-  chunk_rank(a, 0, s, loc, rank);
+  int loc[PER], rank[PER];
+  chunk_rank<PER>(a, 0, s, loc, rank);
   int* base = sm_base(s, a.E);
   for (int e = threadIdx.x; e < a.E; e += kThreads) base[e] = 0;
   __syncthreads();
-  scatter_chunk(a, 0, s, loc, rank, scan_scratch);
+  scatter_chunk<PER>(a, 0, s, loc, rank, scan_scratch);
 }
 
 // The smallest batches (M * topk <= 32 assignments, e.g. one decode token at
@@ -137,13 +137,21 @@ cudaError_t launch_tiny(const RouteIn& r, const AlignArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int EPL, int PER>
+cudaError_t launch_fused_per(const RouteIn& r, const AlignArgs& a, cudaStream_t st) {
+  const size_t smem = align_smem_bytes(a.E);
+  cudaError_t err = ensure_smem_limit<route_align_kernel<EPL, PER>>(static_cast<int>(align_smem_bytes(1024)));
+  if (err != cudaSuccess) return err;
+  route_align_kernel<EPL, PER><<<1, kThreads, smem, st>>>(r, a);
+  return cudaGetLastError();
+}
 template <int EPL>
 cudaError_t launch_fused(const RouteIn& r, const AlignArgs& a, cudaStream_t st) {
-  const size_t smem = align_smem_bytes(a.E);
-  cudaError_t err = ensure_smem_limit<route_align_kernel<EPL>>(static_cast<int>(align_smem_bytes(1024)));
-  if (err != cudaSuccess) return err;
-  route_align_kernel<EPL><<<1, kThreads, smem, st>>>(r, a);
-  return cudaGetLastError();
+  switch (align_per_thread(a.n)) {
+    case 1: return launch_fused_per<EPL, 1>(r, a, st);
+    case 2: return launch_fused_per<EPL, 2>(r, a, st);
+    default: return launch_fused_per<EPL, kPerThread>(r, a, st);
+  }
 }
 
 }  // namespace
