@@ -24,9 +24,11 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kVecInFlight = 16;   // 16-byte vectors a thread loads before adding
 
-// kOrdered: a programmatic launch; y, w and pos come from kernels that may
-// still be running when this grid starts, so they are read after the wait
-// with ordered L2 loads (see grid_dep_wait), not through the read-only cache.
+// kOrdered: a programmatic launch.  y comes from the kernel this one waits
+// for, so it is read after the wait; w and pos from earlier kernels of the
+// chain, already complete when this grid starts, so they are read before it.
+// Both with ordered L2 loads (see grid_dep_wait), not through the read-only
+// cache.
 // A position at or past y_rows counts as no assignment, so a position map
 // that a failed earlier kernel left unwritten cannot send a load out of y.
 template <bool kOrdered, int VPT>
@@ -37,9 +39,11 @@ __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* y, co
   __shared__ int s_pos[32];
   __shared__ float s_w[32];
   __shared__ int s_nloc;
-  grid_dep_wait();
-  grid_dep_launch();
   const int t = blockIdx.x, tid = threadIdx.x;
+  // The positions and weights come from the router and the align, which
+  // completed before the kernel this one waits for started (each kernel of
+  // the chain waits for the one before it), so they are read before the
+  // wait; only y, the kernel before's output, is read after it.
   if (tid < 32) {
     int p = -1;
     float wj = 0.f;
@@ -58,6 +62,8 @@ __global__ void __launch_bounds__(kThreads) moe_sum_kernel(const uint16_t* y, co
     }
     if (tid == 0) s_nloc = __popc(local);
   }
+  grid_dep_wait();
+  grid_dep_launch();
   __syncthreads();
   const int nloc = s_nloc;
   const int v0 = blockIdx.y * kThreads * VPT;
