@@ -285,12 +285,18 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     int nblocks = 0;
     SItem first{0, 0, 0, -1, 1, 0, 0, 0, 0};
     int pre = 0;   // stages of the first item's first pass already issued
+    int i_early = -1;   // mode 1: the first item number, taken before the wait
     if (a.pdl == 2) {
       // The expert map is read from L2 here, never from a copy an SM cached
       // before it was written.
       nblocks = ld_cg(a.ntpp) / a.block_m;
     } else {
       if (a.pdl) {
+        // The work counter was cleared before the kernel this one waits for
+        // started, so the first item number is claimed now and its round
+        // trip overlaps the wait; the item is decoded after it.
+        if (lane == 0 && !a.test_timeout) i_early = atomicAdd(a.work, 1);
+        i_early = __shfl_sync(0xffffffffu, i_early, 0);
         grid_dep_wait();
         grid_dep_launch();
       }
@@ -342,12 +348,18 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
         use_first = false;
       } else {
         if (held_k == held_n) {
-          int i = 0;
-          if (lane == 0) i = atomicAdd(a.work, batch);
-          i = __shfl_sync(0xffffffffu, i, 0);
-          held = decode_item(lane < batch ? i + lane : static_cast<int>(total), total, nblocks, nsplit, how);
+          int i = 0, nb = batch;
+          if (i_early >= 0) {
+            i = i_early;
+            nb = 1;
+            i_early = -1;
+          } else {
+            if (lane == 0) i = atomicAdd(a.work, batch);
+            i = __shfl_sync(0xffffffffu, i, 0);
+          }
+          held = decode_item(lane < nb ? i + lane : static_cast<int>(total), total, nblocks, nsplit, how);
           held_k = 0;
-          held_n = batch;
+          held_n = nb;
         }
         item.tile = __shfl_sync(0xffffffffu, held.tile, held_k);
         item.e = __shfl_sync(0xffffffffu, held.e, held_k);
