@@ -128,6 +128,14 @@ def test_align_layer_workloads(shape):
     (3, 2, 4, 0, 4, 128),
     (40, 4, 1024, 0, 1024, 16),     # widest shard
     (6000, 6, 16, 0, 16, 64),       # heavy per-expert counts over 9 chunks
+    # one chunk, by assignments per thread (512 threads): 1 (n <= 512), 2
+    # (n <= 1024), 8; and by the cross-warp prefix: lane scans (E_local <= 64)
+    # or a loop per expert
+    (64, 8, 384, 0, 48, 8),         # n = 512, 1 per thread, lane scans
+    (65, 8, 384, 0, 48, 8),         # n = 520, 2 per thread
+    (128, 8, 384, 0, 64, 16),       # n = 1024, 2 per thread, E_local = 64
+    (129, 8, 384, 0, 65, 16),       # n = 1032, 8 per thread, loop prefix
+    (250, 8, 384, 16, 48, 16),      # n = 2000, 8 per thread, lane scans
 ])
 def test_align_edge_shapes(M, k, E, begin, E_local, bm):
     logits, bias = wl.router_inputs(M, E, 31)
