@@ -358,7 +358,8 @@ int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t*
  *                copies of the routing (may be NULL)
  *   workspace    chord_moe_layer_workspace_bytes() bytes, 16-byte aligned,
  *                any contents (every call's first kernel clears the
- *                counters the later kernels use); it holds the routing, the align buffers, h, y,
+ *                counters the later kernels use); it holds the routing,
+ *                the align buffers, h, y,
  *                and the GEMMs' work-queue and split-K state
  * The expert-parallel shard is implied by E_local < E_total ([Chord]
  * "런타임 고려사항": the profile is inferred from the shapes, no shard
