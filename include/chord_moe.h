@@ -174,7 +174,7 @@ int chord_moe_route_align(const float* logits, const float* bias, int M, int E_t
  * Arguments, outputs and results are those of chord_moe_align; the only
  * difference is where the scratch lives: when M*topk > 4096 the align needs
  * per-assignment ranks and per-chunk counts, and this entry point keeps them
- * in one static device array inside the library (320 KiB, held by every GPU
+ * in one static device array inside the library (512 KiB, held by every GPU
  * that loads the library until the process exits) instead of a workspace.
  *   Limits: M*topk <= CHORD_ALIGN_NOALLOC_MAX_ASSIGNMENTS and
  *   E_local <= CHORD_ALIGN_NOALLOC_MAX_EXPERTS; larger calls return

@@ -55,7 +55,7 @@ def test_sizing_functions(L):
     assert L.chord_moe_align_capacity(64, 8, 48, 16) == 512 + 48 * 15
     assert L.chord_moe_align_capacity(1, 8, 384, 7) == 0           # bad block_m
     assert L.chord_moe_align_workspace_bytes(128, 8, 384) == 0      # one chunk: none
-    assert L.chord_moe_align_workspace_bytes(4096, 8, 384) == (32768 + 8 * 384) * 4
+    assert L.chord_moe_align_workspace_bytes(4096, 8, 384) == (32768 + 32 * 384) * 4   # chunks of 1024
     assert L.chord_w4a16_prepack_bytes(48, 4096, 7168, 32) == 256 + 48 * 64 * 112 * 2304
     assert L.chord_w4a16_prepack_bytes(1, 16, 64, 32) == 256 + 2304
     assert L.chord_w4a16_prepack_bytes(1, 16, 96, 32) == 0          # K % 64

@@ -123,11 +123,11 @@ def test_align_layer_workloads(shape):
 
 
 @pytest.mark.parametrize("M,k,E,begin,E_local,bm", [
-    (1000, 8, 384, 96, 48, 8),      # two chunks, ragged, EP shard
-    (513, 8, 384, 0, 384, 32),      # just over one chunk
+    (1000, 8, 384, 96, 48, 8),      # 8000 assignments: 8 chunks of 1024, ragged, EP shard
+    (513, 8, 384, 0, 384, 32),      # 4104: just over one CTA's 4096, 5 chunks
     (3, 2, 4, 0, 4, 128),
     (40, 4, 1024, 0, 1024, 16),     # widest shard
-    (6000, 6, 16, 0, 16, 64),       # heavy per-expert counts over 9 chunks
+    (6000, 6, 16, 0, 16, 64),       # heavy per-expert counts over 36 chunks
     # one chunk, by assignments per thread (512 threads): 1 (n <= 512), 2
     # (n <= 1024), 8; and by the cross-warp prefix: lane scans (E_local <= 64)
     # or a loop per expert

@@ -26,23 +26,25 @@ __global__ void __launch_bounds__(kThreads) align_single_kernel(AlignArgs a) {
   scatter_chunk<PER>(a, 0, s, loc, rank, scan_scratch);
 }
 
+template <int PER>
 __global__ void __launch_bounds__(kThreads) align_rank_kernel(AlignArgs a) {
   extern __shared__ int s[];
   const int g = blockIdx.x;
-  int loc[kPerThread], rank[kPerThread];
+  int loc[PER], rank[PER];
   grid_dep_wait();
   grid_dep_launch();
-  chunk_rank(a, g, s, loc, rank);
+  chunk_rank<PER>(a, g, s, loc, rank);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-  for (int step = 0; step < kPerThread; ++step) {
-    const int idx = elem_index(g, warp, step, lane);
+  for (int step = 0; step < PER; ++step) {
+    const int idx = elem_index<PER>(g, warp, step, lane);
     if (idx < a.n) a.ws_rank[idx] = rank[step];
   }
   int* tot = sm_tot(s, a.E);
   for (int e = threadIdx.x; e < a.E; e += kThreads) a.ws_counts[g * a.E + e] = tot[e];
 }
 
+template <int PER>
 __global__ void __launch_bounds__(kThreads) align_scatter_kernel(AlignArgs a) {
   extern __shared__ int s[];
   __shared__ int scan_scratch[kWarps + 1];
@@ -62,10 +64,10 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(AlignArgs a) {
     tot[e] = t;
     base[e] = b;
   }
-  int loc[kPerThread], rank[kPerThread];
+  int loc[PER], rank[PER];
 #pragma unroll
-  for (int step = 0; step < kPerThread; ++step) {
-    const int idx = elem_index(g, warp, step, lane);
+  for (int step = 0; step < PER; ++step) {
+    const int idx = elem_index<PER>(g, warp, step, lane);
     loc[step] = -1;
     rank[step] = 0;
     if (idx < a.n) {
@@ -77,13 +79,15 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(AlignArgs a) {
     }
   }
   __syncthreads();
-  scatter_chunk(a, g, s, loc, rank, scan_scratch);
+  scatter_chunk<PER>(a, g, s, loc, rank, scan_scratch);
 }
 
 
 }  // namespace
 
-int align_num_chunks(long long n) { return n <= kChunk ? 1 : static_cast<int>((n + kChunk - 1) / kChunk); }
+int align_num_chunks(long long n) {
+  return n <= kChunk ? 1 : static_cast<int>((n + kMultiChunk - 1) / kMultiChunk);
+}
 
 size_t align_workspace_bytes(long long n, int E_local) {
   const int G = align_num_chunks(n);
@@ -115,8 +119,8 @@ cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_l
   cudaError_t err = ensure_smem_limit<align_single_kernel<1>>(max_smem);
   if (err == cudaSuccess) err = ensure_smem_limit<align_single_kernel<2>>(max_smem);
   if (err == cudaSuccess) err = ensure_smem_limit<align_single_kernel<kPerThread>>(max_smem);
-  if (err == cudaSuccess) err = ensure_smem_limit<align_rank_kernel>(max_smem);
-  if (err == cudaSuccess) err = ensure_smem_limit<align_scatter_kernel>(max_smem);
+  if (err == cudaSuccess) err = ensure_smem_limit<align_rank_kernel<kMultiPer>>(max_smem);
+  if (err == cudaSuccess) err = ensure_smem_limit<align_scatter_kernel<kMultiPer>>(max_smem);
   if (err != cudaSuccess) return err;
   if (a.G == 1) {
     switch (align_per_thread(a.n)) {
@@ -125,9 +129,9 @@ cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_l
       default: return launch_kernel(align_single_kernel<kPerThread>, dim3(1), dim3(kThreads), smem, st, pdl, a);
     }
   }
-  err = launch_kernel(align_rank_kernel, dim3(a.G), dim3(kThreads), smem, st, pdl, a);
+  err = launch_kernel(align_rank_kernel<kMultiPer>, dim3(a.G), dim3(kThreads), smem, st, pdl, a);
   if (err != cudaSuccess) return err;
-  align_scatter_kernel<<<a.G, kThreads, smem, st>>>(a);
+  align_scatter_kernel<kMultiPer><<<a.G, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -137,14 +141,14 @@ cudaError_t align_launch(const int32_t* ids, int M, int topk, int begin, int E_l
 // Allocation-free align: the scratch of the multi-chunk path (per-assignment
 // chunk ranks, then per-chunk expert counts) lives in this file-scope device
 // array instead of a caller-provided workspace.  Every GPU that loads the
-// library holds it (320 KiB) until the process exits.
+// library holds it (512 KiB) until the process exits.
 namespace chord {
 
 constexpr long long kNoAllocMaxAssignments = CHORD_ALIGN_NOALLOC_MAX_ASSIGNMENTS;
 constexpr int kNoAllocMaxExperts = CHORD_ALIGN_NOALLOC_MAX_EXPERTS;
 constexpr long long kNoAllocScratchInts =
     kNoAllocMaxAssignments +
-    ((kNoAllocMaxAssignments + kChunk - 1) / kChunk) * static_cast<long long>(kNoAllocMaxExperts);
+    ((kNoAllocMaxAssignments + kMultiChunk - 1) / kMultiChunk) * static_cast<long long>(kNoAllocMaxExperts);
 
 static __device__ __align__(256) int32_t g_align_scratch[kNoAllocScratchInts];
 

@@ -26,7 +26,11 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPerThread = 8;
-constexpr int kChunk = kThreads * kPerThread;  // 4096 assignments per CTA
+constexpr int kChunk = kThreads * kPerThread;  // 4096: the most one CTA aligns alone
+// Above kChunk assignments the align runs in chunks of kThreads * kMultiPer
+// (1024) over as many CTAs: more CTAs, each with fewer serial steps.
+constexpr int kMultiPer = 2;
+constexpr int kMultiChunk = kThreads * kMultiPer;
 
 struct AlignArgs {
   const int32_t* ids;
@@ -44,7 +48,7 @@ __device__ __forceinline__ int* sm_off(int* s, int E) { return s + (kWarps + 2) 
 
 template <int PER = kPerThread>
 __device__ __forceinline__ int elem_index(int g, int warp, int step, int lane) {
-  return g * kChunk + warp * (32 * PER) + step * 32 + lane;
+  return g * (kThreads * PER) + warp * (32 * PER) + step * 32 + lane;
 }
 
 // Elements per thread of a one-chunk align of n assignments.
