@@ -30,7 +30,9 @@ the timed region lasts under a second, else the sustained one).
 
 `e2e` repeats the measurement through the public single call
 (chord_moe_layer) with pinned HOST inputs and outputs: each step copies x
-and the router logits host->device and the layer output device->host.
+and the router logits host->device and the layer output device->host, on
+two copy streams, so the copies of neighbouring steps overlap a step's
+kernels.
 
 `--impl reference` times the CPU oracle (numpy, FP64) on the host cores on a
 bounded sample of the same workload.
@@ -458,15 +460,41 @@ def measure_workload(shape, steps, warmup, R, world, rank, local, seed_base, e2e
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
+    # Every step copies its inputs host->device and its output device->host
+    # inside the timed region.  The copies run on two side streams, so step
+    # i+1's inputs and step i-1's output move while step i computes (the
+    # replicas' buffers rotate, and events order each copy against the steps
+    # that use the same buffers), as a serving loop would pipeline them.
+    main = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(R)]
+    computed = [torch.cuda.Event() for _ in range(R)]
+    out_read = [torch.cuda.Event() for _ in range(R)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    e0.record(main)
+    h2d_s.wait_stream(main)
+    d2h_s.wait_stream(main)
     for i in range(e2e_steps):
-        r = reps[i % R]
-        r.x.copy_(r.x_pinned, non_blocking=True)
-        r.logits.copy_(r.logits_pinned, non_blocking=True)
+        k = i % R
+        r = reps[k]
+        with torch.cuda.stream(h2d_s):
+            if i >= R:
+                h2d_s.wait_event(computed[k])   # the step that last read these buffers is done
+            r.x.copy_(r.x_pinned, non_blocking=True)
+            r.logits.copy_(r.logits_pinned, non_blocking=True)
+            in_ready[k].record(h2d_s)
+        main.wait_event(in_ready[k])
+        if i >= R:
+            main.wait_event(out_read[k])        # the output buffer's last read is done
         r.layer.forward(r.x, r.logits, r.bias, out=r.out)
-        outs_pinned[i % R].copy_(r.out, non_blocking=True)
-    e1.record()
+        computed[k].record(main)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(computed[k])
+            outs_pinned[k].copy_(r.out, non_blocking=True)
+            out_read[k].record(d2h_s)
+    main.wait_stream(d2h_s)
+    main.wait_stream(h2d_s)
+    e1.record(main)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = allreduce_max(e0.elapsed_time(e1), world)
@@ -474,7 +502,9 @@ def measure_workload(shape, steps, warmup, R, world, rank, local, seed_base, e2e
     d2h = shape.M * shape.H * 2
     e2e = {"value": shape.M * e2e_steps * world / (e2e_ms / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-           "api": "chord_moe_layer"}
+           "api": "chord_moe_layer",
+           "copies": "every step's inputs in and output out, on two copy streams overlapping the "
+                     "neighbouring steps' kernels"}
     for r in reps:
         assert r.status.item() == 0 and r.layer.dev_status.item() == 0, "device status after timing"
 
