@@ -6,11 +6,11 @@
 // num_tokens_post_padded, expert_counts, expert_offsets; the per-expert
 // scatter cursors are re-initialised on entry as in "커널 내부 로직 변경").
 //
-// Each CTA owns a chunk of 4096 consecutive assignments; each of its 16
-// warps owns 256 consecutive ones, walked in 8 steps of 32 (PER = 8).  A
-// one-chunk align of at most 512 or 1024 assignments spreads them over all
-// 16 warps instead (PER = 1 or 2: 32 or 64 per warp), so each warp walks one
-// or two steps.  Within a step,
+// Each CTA owns a chunk of 512 * PER consecutive assignments; each of its 16
+// warps owns 32 * PER consecutive ones, walked in PER steps of 32.  One CTA
+// aligns up to 4096 assignments alone (PER = 1, 2 or 8 for at most 512,
+// 1024 or 4096); above that the assignments are split into chunks of 1024
+// (PER = 2), one CTA each, in two phases.  Within a step,
 // __match_any_sync groups lanes with the same expert, the lowest lane of the
 // group advances the warp's counter for that expert, and each lane's rank is
 // the counter's old value plus the number of earlier lanes in its group.  An
