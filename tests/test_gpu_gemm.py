@@ -85,6 +85,10 @@ CASES = [
     (1200, 256, 256, 4, 4, 0, 2, STORE, 16, (SMALL, LARGE)),      # ~600 rows: 3 tcgen05 passes
     (2, 128, 128, 4, 4, 0, 1, STORE, 8, (SMALL, LARGE)),
     (96, 1024, 128, 32, 32, 0, 6, SILU, 8, (SMALL, LARGE)),       # Zipf skew: one heavy expert
+    # short K, 8 rows per pass: items of two weight tiles (K = 256: the
+    # straight-line stage) or four (K = 128), and a last item with fewer tiles
+    (8, 256, 320, 16, 16, 0, 2, STORE, 8, (SMALL,)),
+    (8, 128, 576, 16, 16, 0, 2, SILU, 8, (SMALL,)),
 ]
 
 

@@ -164,6 +164,28 @@ __device__ __forceinline__ void unit_mma(uint32_t ub, uint32_t xu, uint32_t q_of
   }
 }
 
+// One stage of an item of NTL weight tiles of NU units each (K = 64 NU <=
+// 512): straight-line code, so the loads and MMAs of all the tiles' units
+// interleave (the run-time loops it replaces left TP8's K = 256 down GEMM
+// waiting on each unit's loads: 72.9 -> 67.9 us).  Only K = 256 at one
+// token tile per pass, outside the SiLU*mul kernels, takes it: compiled into
+// those (or a second form for K = 128) it raised their register spills.
+template <int NU, int NTL, int NT>
+__device__ __forceinline__ void multi_tile_stage(uint32_t st, uint32_t x_off, uint32_t q_off, uint32_t s_off,
+                                                 const SmallArgs& a, float (&acc)[NTL][NT][4]) {
+#pragma unroll
+  for (int t = 0; t < NTL; ++t)
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[t][n][i] = 0.f;
+#pragma unroll
+  for (int u = 0; u < NU; ++u)
+#pragma unroll
+    for (int t = 0; t < NTL; ++t)
+      unit_mma<NT>(st + (t * NU + u) * kUnitBytes, st + x_off + u * kUnitK * 2, q_off, s_off, a, acc[t]);
+}
+
 template <int NT, int STAGES, bool GATHER, int EPI>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gemm_small_kernel(SmallArgs a) {
   using Cfg = SmallCfg<NT>;
@@ -471,6 +493,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
         const int s = it % STAGES;
         if (!mbar_wait(&full_bar[s], (it / STAGES) & 1, a.status, a.wait_polls)) return;
         const uint32_t st = smem_base + s * Cfg::kStageBytes;
+        const size_t r0 = static_cast<size_t>(item.row0) + pass * Cfg::kRowsPerPass;
+        if (NT == 1 && EPI != CHORD_EPI_SILU_MUL && n_units == 4 && item.ntl == 2) {   // K = 256 (down GEMMs)
+          float acc[2][NT][4];
+          multi_tile_stage<4, 2, NT>(st, x_off, q_off, s_off, a, acc);
+          epilogue(item.tile, acc[0], rows, r0);
+          epilogue(item.tile + 1, acc[1], rows, r0);
+        } else
 #pragma unroll 1
         for (int tl = 0; tl < item.ntl; ++tl) {
           float acc[NT][4];
