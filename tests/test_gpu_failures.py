@@ -38,7 +38,7 @@ def _run(x, packed, E, N, K, M, topk, up, bm, C, ws, status):
 
 
 def test_wait_timeout_is_reported_and_the_next_call_is_exact():
-    # enough work items (32 tiles x ~50 blocks) that the GEMM does not split K
+    # enough work items (32 tiles x ~50 blocks) that the GEMM does not split every item along K
     M, K, N, E, topk, bm = 200, 1024, 2048, 8, 2, 8
     ids, al, x, q, s = _problem(M, K, N, E, E, 0, topk, 71, bm)
     up = _upload_align(al, M, topk, E, bm)

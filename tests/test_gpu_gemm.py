@@ -223,6 +223,48 @@ def test_gemm_split_k_counters_and_parity():
     assert np.array_equal(outs[0][:n].view(np.uint16), outs[1][:n].view(np.uint16))
 
 
+@pytest.mark.parametrize("E,K,extra", [(16, 4096, 0.6), (4, 7168, 0.55)])
+def test_gemm_tail_wave_split_k(E, K, extra):
+    """More work items than resident CTAs, with a last wave of about `extra`
+    of the CTAs (more than half): the decode GEMM takes the other items whole
+    and splits those of the last wave along K (into three ranges over eight
+    stages at 0.6 of a wave, five over fourteen at 0.55).  Every row matches
+    the oracle, split partials were written, the counters are back at zero,
+    and a second call gives the same bits."""
+    M, topk, bm = 64, 2, 8
+    logits, bias = wl.router_inputs(M, E, 43)
+    _, ids, _ = oracle.route(logits, bias, topk)
+    nblocks = oracle.moe_align(ids, 0, E, bm)["num_tokens_post_padded"] // bm
+    ctas = 4 * torch.cuda.get_device_properties(0).multi_processor_count   # resident at 8 rows per pass
+    N = 64 * -(-int(ctas * (1 + extra)) // nblocks)
+    ids, al, x, q, s = _problem(M, K, N, E, E, 0, topk, 43, bm)
+    assert al["num_tokens_post_padded"] // bm == nblocks
+    up = _upload_align(al, M, topk, E, bm)
+    cap = up[0]
+    packed = prepack(to_device(q), to_device(s), False)
+    ws = torch.zeros(chord.chord_w4a16_moe_gemm_workspace_bytes(cap, K, True), dtype=torch.uint8, device="cuda")
+    tun = chord.chord_tuning(SMALL, 8, 0, 0)
+    refs = _oracle_rows(x, q, s, al, topk, STORE, True)
+    outs = []
+    for _ in range(2):
+        C = torch.full((cap, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        chord.chord_w4a16_moe_gemm(to_device(x), True, packed, E, N, K, M, topk, *up[1:], bm, STORE, C, ws,
+                                   tuning=tun, dev_status=status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        assert int(ws[256:256 + 512 * 4 * 4].view(torch.int32).abs().sum().item()) == 0, \
+            "split-K counters must be left at zero"
+        assert int(ws[:256].view(torch.int32).abs().sum().item()) == 0
+        partials = ws[256 + 512 * 16:256 + 512 * 16 + 512 * 2048 * 4]
+        assert int((partials != 0).sum().item()) > 0, "the last wave was not split"
+        outs.append(bf16_to_np(C))
+        for e, (rows, ref) in refs.items():
+            assert_close_to_oracle(outs[-1][rows], ref, f"tail split expert {e}", *GEMM_TOL[SMALL])
+    n = al["num_tokens_post_padded"]
+    assert np.array_equal(outs[0][:n].view(np.uint16), outs[1][:n].view(np.uint16))
+
+
 @pytest.mark.parametrize("path", [SMALL, LARGE])
 @pytest.mark.parametrize("M,K,N,E,topk,bm", [(40, 256, 384, 6, 3, 16), (300, 512, 256, 4, 2, 16)])
 def test_weighted_add_epilogue(path, M, K, N, E, topk, bm):

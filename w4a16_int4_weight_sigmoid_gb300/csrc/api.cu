@@ -668,10 +668,12 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
   chord_bf16* h = reinterpret_cast<chord_bf16*>(ws + w.h);
   chord_bf16* y = reinterpret_cast<chord_bf16*>(ws + w.y);
 
-  // Register-MMA path: every kernel after the router is a programmatic
-  // launch, so its launch and prologue overlap the end of the kernel before
-  // it, and the down GEMM streams its first weight stages while the gate/up
-  // GEMM finishes.  The tcgen05 path launches in plain stream order.
+  // The router is a programmatic launch on both paths (it touches nothing
+  // before the work ahead of the call has completed).  Register-MMA path:
+  // every later kernel is one too, so its launch and prologue overlap the
+  // end of the kernel before it, and the down GEMM streams its first weight
+  // stages while the gate/up GEMM finishes.  The tcgen05 path launches its
+  // later kernels in plain stream order.
   const bool pdl = plan.path != CHORD_PATH_LARGE_M;
   // one launch when the assignments fit one align chunk, else two
   // The router kernel (the layer's first) clears both GEMMs' work-queue and

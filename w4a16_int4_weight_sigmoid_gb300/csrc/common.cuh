@@ -67,6 +67,11 @@ __device__ __forceinline__ int ld_ca(const int32_t* p) {
   asm volatile("ld.global.ca.b32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
+__device__ __forceinline__ float ld_ca(const float* p) {
+  float v;
+  asm volatile("ld.global.ca.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ float ld_cg(const float* p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));

@@ -39,7 +39,11 @@
 //     only where the grid is not already full): when a launch has at most
 //     half as many items as resident CTAs (a few decode tokens touching one
 //     or two experts), every item is split into S <= 8 ranges of K stages so
-//     that all CTAs stream weights.  Each split writes its FP32 partial
+//     that all CTAs stream weights.  Otherwise, when the last, partial wave
+//     (n mod CTAs of n items, handed out last) fills more than half of the
+//     CTAs, its items are split, into as many ranges as make that wave
+//     shortest, so the launch does not end on a whole item's time with its
+//     CTAs sharing the SMs.  Each split writes its FP32 partial
 //     accumulators to the workspace; the last split of an item to arrive
 //     (per-item counters, reset by that last arrival) adds the S partials in
 //     split order, so the result does not depend on which CTA finishes last,
@@ -63,6 +67,9 @@ struct SmallCfg {
   static constexpr int kWBytes = kUnitsPerStage * kUnitBytes;
   static constexpr int kXBytes = kRowsPerPass * kXPitch;
   static constexpr int kStageBytes = kWBytes + kXBytes;
+  // FP32 partial accumulators of one split of one item (every consumer lane's)
+  static constexpr int kSlotFloats = kConsumerWarps * 32 * 4 * NT;
+  static constexpr long long kSlots = static_cast<long long>(kSplitPartialBytes / sizeof(float) / kSlotFloats);
 };
 
 constexpr int kItemSlots = 4;
@@ -73,8 +80,15 @@ struct SItem {
   int tile, e, row0, rows;   // first 64-row weight tile, local expert, first sorted row, rows of the block
   int ntl;                   // consecutive weight tiles in the item (several only when K fits one stage)
   int ks0, ks1;              // K stages [ks0, ks1) of this split
-  int base;                  // item index without the split (counter index)
-  int split;                 // split index | (number of splits << 16)
+  int slot;                  // split items: partials at slots [slot * S, slot * S + S), counters of slot
+  int split;                 // split index | (number of splits S << 16)
+};
+
+// How a launch's items split along K: every item into `all` ranges, or the
+// items from `head` on into `tail` ranges each (1: no split).
+struct SplitPlan {
+  int all, tail;
+  long long head;
 };
 
 struct SmallArgs {
@@ -255,15 +269,32 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       return how == 0 ? __ldg(p) : how == 1 ? ld_ca(p) : ld_cg(p);
     };
     const int how = a.pdl ? 1 : 0;   // after the wait
-    // item i -> split s of base item i / S = (tile, block), block index fastest
-    auto decode_item = [&](int i, long long total, int nblocks, int nsplit, int how) {
+    // item i -> split sp of base item (tile group, block), block index fastest
+    auto decode_item = [&](int i, long long total, int nblocks, const SplitPlan& pl, int how) {
       SItem item{0, 0, 0, -1, 1, 0, 0, 0, 0};
       if (i >= 0 && i < total) {   // below zero: counters never zeroed; no item
-        const int base = i / nsplit, sp = i - base * nsplit;
+        int base, sp, ns, slot;
+        if (pl.all > 1) {
+          base = i / pl.all;
+          sp = i - base * pl.all;
+          ns = pl.all;
+          slot = base;
+        } else if (i < pl.head) {
+          base = i;
+          sp = 0;
+          ns = 1;
+          slot = 0;
+        } else {
+          const int j = i - static_cast<int>(pl.head);
+          slot = j / pl.tail;
+          sp = j - slot * pl.tail;
+          ns = pl.tail;
+          base = static_cast<int>(pl.head) + slot;
+        }
         const int ng = base / nblocks, b = base - ng * nblocks;
         const int e = ld_map(a.expert_ids + b, how);
-        item = SItem{ng * tpi, 0, 0, 0, min(tpi, a.n_tiles - ng * tpi), sp * k_stages / nsplit,
-                     (sp + 1) * k_stages / nsplit, base, sp | (nsplit << 16)};
+        item = SItem{ng * tpi, 0, 0, 0, min(tpi, a.n_tiles - ng * tpi), sp * k_stages / ns,
+                     (sp + 1) * k_stages / ns, slot, sp | (ns << 16)};
         if (e >= 0 && e < a.E_local) {
           const int row0 = b * a.block_m;
           const int end = ld_map(a.offsets + e, how) + ld_map(a.counts + e, how);
@@ -328,23 +359,47 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
       set_status(a.status, CHORD_ERR_INVALID_ARG);
       nblocks = nblocks < 0 ? 0 : a.max_blocks;
     }
-    // split-K when the grid is not saturated: at most half as many items
-    // as CTAs, one pass per item, a split workspace and more than one stage
+    // split-K needs one pass per item, a split workspace and more than one
+    // stage.  At most half as many items as CTAs: every item splits.  Else,
+    // when the last wave holds r = n mod CTAs > CTAs / 2 items, those split
+    // into S ranges of at least two stages (S <= kMaxSplit, the partial
+    // slots), S giving the shortest last wave if shorter than one item:
+    // ceil(r S / CTAs) rounds of ceil(stages / S) stages, each range costing
+    // about half a stage more (its partials' round trip).  Measured on GB300:
+    // TP8 decode gate/up (r ~ 0.6 of the CTAs, S = 3 or 5) 108.2 -> 106.4 us;
+    // below half a wave (EP8 decode gate/up, r ~ 0.3-0.4) or with one-stage
+    // ranges (EP8 down, S = 4) splitting was slower (76.6 -> 77.3 us,
+    // 43.3 -> 45.5 us): CTAs of a thin last wave share their SMs with few
+    // others and finish early anyway.
     const long long n_base = static_cast<long long>(n_groups) * nblocks;
-    int nsplit = 1;
-    if (a.partial && a.block_m <= Cfg::kRowsPerPass && k_stages > 1 && n_base > 0 &&
-        2 * n_base <= static_cast<long long>(gridDim.x)) {
-      nsplit = static_cast<int>(min(static_cast<long long>(gridDim.x) / n_base,
-                                    static_cast<long long>(min(k_stages, kMaxSplit))));
-      nsplit = static_cast<int>(min(static_cast<long long>(nsplit), kSplitSlots / n_base));
-      if (nsplit < 2) nsplit = 1;
+    const long long ctas = gridDim.x;
+    SplitPlan plan{1, 1, n_base};
+    if (a.partial && a.block_m <= Cfg::kRowsPerPass && k_stages > 1 && n_base > 0) {
+      if (2 * n_base <= ctas) {
+        int nsplit = static_cast<int>(min(ctas / n_base, static_cast<long long>(min(k_stages, kMaxSplit))));
+        nsplit = static_cast<int>(min(static_cast<long long>(nsplit), kSplitSlots / n_base));
+        plan.all = nsplit < 2 ? 1 : nsplit;
+      } else {
+        const long long r = n_base % ctas;
+        if (2 * r > ctas && r <= kSplitSlots) {
+          long long best = 2LL * k_stages;   // the last wave in half stages, unsplit
+          for (int S = 2; S <= min(k_stages / 2, kMaxSplit) && r * S <= Cfg::kSlots; ++S) {
+            const long long len = (r * S + ctas - 1) / ctas * (2LL * ((k_stages + S - 1) / S) + 1);
+            if (len < best) {
+              best = len;
+              plan.tail = S;
+            }
+          }
+          if (plan.tail > 1) plan.head = n_base - r;
+        }
+      }
     }
-    const long long total = n_base * nsplit;
+    const long long total = plan.all > 1 ? n_base * plan.all : plan.head + (n_base - plan.head) * plan.tail;
     if (a.pdl == 2) {
       int i = 0;
       if (lane == 0 && !a.test_timeout) i = atomicAdd(a.work, 1);
       i = __shfl_sync(0xffffffffu, i, 0);
-      first = decode_item(a.test_timeout ? static_cast<int>(total) : i, total, nblocks, nsplit, 2);
+      first = decode_item(a.test_timeout ? static_cast<int>(total) : i, total, nblocks, plan, 2);
       const int rows0 = min(Cfg::kRowsPerPass, first.rows);
       if (rows0 > 0) {
         pre = min(STAGES, first.ks1 - first.ks0);
@@ -360,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
     // and the expert map, so they are taken two at a time: lane j decodes
     // item base + j, and the loop hands them out in order (TP8 down GEMM
     // 73.8 -> 72.2 us; four or eight at a time measured no better or worse).
-    const int batch = (k_stages + nsplit - 1) / nsplit <= 1 ? 2 : 1;
+    const int batch = (k_stages + plan.all - 1) / plan.all <= 1 ? 2 : 1;
     SItem held{0, 0, 0, -1, 1, 0, 0, 0, 0};
     int held_k = 0, held_n = 0;
     while (ok) {
@@ -379,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
             if (lane == 0) i = atomicAdd(a.work, batch);
             i = __shfl_sync(0xffffffffu, i, 0);
           }
-          held = decode_item(lane < nb ? i + lane : static_cast<int>(total), total, nblocks, nsplit, how);
+          held = decode_item(lane < nb ? i + lane : static_cast<int>(total), total, nblocks, plan, how);
           held_k = 0;
           held_n = nb;
         }
@@ -390,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
         item.ntl = __shfl_sync(0xffffffffu, held.ntl, held_k);
         item.ks0 = __shfl_sync(0xffffffffu, held.ks0, held_k);
         item.ks1 = __shfl_sync(0xffffffffu, held.ks1, held_k);
-        item.base = __shfl_sync(0xffffffffu, held.base, held_k);
+        item.slot = __shfl_sync(0xffffffffu, held.slot, held_k);
         item.split = __shfl_sync(0xffffffffu, held.split, held_k);
         ++held_k;
       }
@@ -547,19 +602,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
         // split-K (one pass per item): publish this split's partial, and
         // the last split of the item to arrive adds all of them in split
         // order and runs the epilogue
-        float* slot_base = a.partial + static_cast<size_t>(item.base) * nsplit * kSplitSlotFloats;
-        float4* mine = reinterpret_cast<float4*>(slot_base + static_cast<size_t>(sp) * kSplitSlotFloats +
+        float* slot_base = a.partial + static_cast<size_t>(item.slot) * nsplit * Cfg::kSlotFloats;
+        float4* mine = reinterpret_cast<float4*>(slot_base + static_cast<size_t>(sp) * Cfg::kSlotFloats +
                                                  (warp * 32 + lane) * 4 * NT);
 #pragma unroll
         for (int n = 0; n < NT; ++n) mine[n] = make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
         __threadfence();
         __syncwarp();
         int prev = 0;
-        if (lane == 0) prev = atomicAdd(a.split_cnt + item.base * kConsumerWarps + warp, 1);
+        if (lane == 0) prev = atomicAdd(a.split_cnt + item.slot * kConsumerWarps + warp, 1);
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev != nsplit - 1) continue;   // not the last split of this item
         __threadfence();
-        if (lane == 0) atomicExch(a.split_cnt + item.base * kConsumerWarps + warp, 0);   // ready for the next launch
+        if (lane == 0) atomicExch(a.split_cnt + item.slot * kConsumerWarps + warp, 0);   // ready for the next launch
         float sum[NT][4];
         for (int k = 0; k < nsplit; ++k) {
 #pragma unroll
@@ -568,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 2 ? 3 : 2)) gem
             if (k == sp) {
               v = make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
             } else {
-              v = ld_cg_f4(slot_base + static_cast<size_t>(k) * kSplitSlotFloats + (warp * 32 + lane) * 4 * NT + 4 * n);
+              v = ld_cg_f4(slot_base + static_cast<size_t>(k) * Cfg::kSlotFloats + (warp * 32 + lane) * 4 * NT + 4 * n);
             }
             if (k == 0) {
               sum[n][0] = v.x; sum[n][1] = v.y; sum[n][2] = v.z; sum[n][3] = v.w;

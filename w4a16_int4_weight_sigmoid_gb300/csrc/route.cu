@@ -27,8 +27,8 @@ cudaError_t launch_route(const float* logits, const float* bias, int M, int E, i
                          float* w, int32_t* ids, cudaStream_t st, int* zero, int n_zero) {
   const int warps = 4;
   const int grid = (M + warps - 1) / warps;
-  route_kernel<EPL><<<grid, warps * 32, 0, st>>>(logits, bias, M, E, topk, w, ids, zero, n_zero);
-  return cudaGetLastError();
+  return launch_kernel(route_kernel<EPL>, dim3(grid), dim3(warps * 32), 0, st, true, logits, bias, M, E, topk,
+                       w, ids, zero, n_zero);
 }
 
 }  // namespace

@@ -133,8 +133,7 @@ __global__ void __launch_bounds__(32 * kTinyMaxWarps) route_align_tiny_kernel(Ro
 template <int EPL>
 cudaError_t launch_tiny(const RouteIn& r, const AlignArgs& a, cudaStream_t st) {
   const int warps = r.M > kTinyWarps ? (r.M < kTinyMaxWarps ? r.M : kTinyMaxWarps) : kTinyWarps;
-  route_align_tiny_kernel<EPL><<<1, 32 * warps, 0, st>>>(r, a);
-  return cudaGetLastError();
+  return launch_kernel(route_align_tiny_kernel<EPL>, dim3(1), dim3(32 * warps), 0, st, true, r, a);
 }
 
 template <int EPL, int PER>
@@ -142,8 +141,7 @@ cudaError_t launch_fused_per(const RouteIn& r, const AlignArgs& a, cudaStream_t 
   const size_t smem = align_smem_bytes(a.E);
   cudaError_t err = ensure_smem_limit<route_align_kernel<EPL, PER>>(static_cast<int>(align_smem_bytes(1024)));
   if (err != cudaSuccess) return err;
-  route_align_kernel<EPL, PER><<<1, kThreads, smem, st>>>(r, a);
-  return cudaGetLastError();
+  return launch_kernel(route_align_kernel<EPL, PER>, dim3(1), dim3(kThreads), smem, st, true, r, a);
 }
 template <int EPL>
 cudaError_t launch_fused(const RouteIn& r, const AlignArgs& a, cudaStream_t st) {

@@ -58,13 +58,16 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, con
   const int lane = threadIdx.x & 31;
   const float* row = logits + static_cast<size_t>(t) * E;
   // All loads first (clamped in-range addresses, no branches), so they are in
-  // flight together instead of one round trip per expert.
+  // flight together instead of one round trip per expert.  Ordered loads:
+  // the kernels calling this are programmatic launches whose logits come from
+  // the kernel before them (see grid_dep_wait); the bias, which every warp
+  // reads, through L1.
   float lg[EPL], bs[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = min(lane + 32 * i, E - 1);
-    lg[i] = __ldg(row + e);
-    bs[i] = __ldg(bias + e);
+    lg[i] = ld_cg(row + e);
+    bs[i] = ld_ca(bias + e);
   }
   uint64_t cand[EPL];
   float sc[EPL];
