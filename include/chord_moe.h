@@ -107,10 +107,11 @@ int chord_version(void);
  * are bit-identical across implementations of the same sequence; key_e =
  * s_e + bias_e; the topk largest keys win, equal keys going to the lower id.
  * Requires 1 <= topk <= min(E_total, 32), 1 <= E_total <= 1024, M >= 0.
- * The router kernel is a programmatic dependent launch that touches no
- * memory before the kernel ahead of it in the stream has completed, so
- * stream order holds; its launch overlaps that kernel (the logits' producer,
- * or the previous call).
+ * Up to 512 tokens the router kernel is a programmatic dependent launch
+ * that touches no memory before the kernel ahead of it in the stream has
+ * completed, so stream order holds while its launch overlaps that kernel
+ * (the logits' producer, or the previous call); above that it is an
+ * ordinary launch.
  */
 int chord_moe_route(const float* logits, const float* bias, int M, int E_total, int topk,
                     float* topk_weights, int32_t* topk_ids, void* stream);
@@ -369,10 +370,10 @@ int chord_moe_sum(const chord_bf16* y, const float* topk_weights, const int32_t*
  * The expert-parallel shard is implied by E_local < E_total ([Chord]
  * "런타임 고려사항": the profile is inferred from the shapes, no shard
  * argument).  Weights are normalised over all topk experts, local or not.
- * Launch order: the first kernel (the router) is a programmatic dependent
- * launch that touches no memory before all earlier work in the stream has
- * completed.  On the register-MMA path every later kernel of the call is one
- * too: it may start before the previous kernel of the call ends and waits
+ * Launch order: the first kernel (the router) is launched as
+ * chord_moe_route's is, so it touches no memory before all earlier work in
+ * the stream has completed.  On the register-MMA path every later kernel of
+ * the call is a programmatic dependent launch: it may start before the previous kernel of the call ends and waits
  * for it before reading its outputs (captured into a CUDA graph, these
  * become programmatic edges).  Work enqueued after the call starts after
  * its last kernel ends.

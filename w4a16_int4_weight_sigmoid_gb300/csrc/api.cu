@@ -668,7 +668,7 @@ int chord_moe_layer(const chord_bf16* x, const float* logits, const float* bias,
   chord_bf16* h = reinterpret_cast<chord_bf16*>(ws + w.h);
   chord_bf16* y = reinterpret_cast<chord_bf16*>(ws + w.y);
 
-  // The router is a programmatic launch on both paths (it touches nothing
+  // The router is a programmatic launch up to 512 tokens (it touches nothing
   // before the work ahead of the call has completed).  Register-MMA path:
   // every later kernel is one too, so its launch and prologue overlap the
   // end of the kernel before it, and the down GEMM streams its first weight

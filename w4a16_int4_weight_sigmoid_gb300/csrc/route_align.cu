@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kThreads) route_align_kernel(RouteIn r, AlignA
   grid_dep_wait();
   grid_dep_launch();
   zero_ints(r.zero, r.n_zero);
-  for (int t = warp; t < r.M; t += kWarps) route_token<EPL>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
+  for (int t = warp; t < r.M; t += kWarps) route_token<EPL, true>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
   __syncthreads();   // this CTA's topk_ids stores are visible to all its threads
   int loc[PER], rank[PER];
   chunk_rank<PER>(a, 0, s, loc, rank);
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(32 * kTinyMaxWarps) route_align_tiny_kernel(Ro
   grid_dep_launch();
   zero_ints(r.zero, r.n_zero);
   for (int t = warp; t < r.M; t += nw) {
-    const int id = route_token<EPL>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
+    const int id = route_token<EPL, true>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
     if (lane < r.topk) s_id[t * r.topk + lane] = id;
   }
   __syncthreads();

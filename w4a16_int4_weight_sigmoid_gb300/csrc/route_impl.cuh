@@ -50,24 +50,24 @@ __device__ __forceinline__ uint64_t pack_key(float key, int id) {
 
 // Route token t with the calling (whole, converged) warp: EPL experts per
 // lane (e = lane + 32 i); writes topk_ids / topk_weights row t and returns,
-// in lanes 0 .. topk-1, the id of that rank.
-template <int EPL>
+// in lanes 0 .. topk-1, the id of that rank.  ORDERED: the caller is a
+// programmatic launch (see grid_dep_wait), so logits and bias are read with
+// ordered loads after its wait instead of __ldg.
+template <int EPL, bool ORDERED>
 __device__ __forceinline__ int route_token(const float* __restrict__ logits, const float* __restrict__ bias,
                                             int t, int E, int topk, float* __restrict__ w_out,
                                             int32_t* __restrict__ id_out) {
   const int lane = threadIdx.x & 31;
   const float* row = logits + static_cast<size_t>(t) * E;
   // All loads first (clamped in-range addresses, no branches), so they are in
-  // flight together instead of one round trip per expert.  Ordered loads:
-  // the kernels calling this are programmatic launches whose logits come from
-  // the kernel before them (see grid_dep_wait); the bias, which every warp
-  // reads, through L1.
+  // flight together instead of one round trip per expert (ordered: the bias,
+  // which every warp reads, through L1).
   float lg[EPL], bs[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = min(lane + 32 * i, E - 1);
-    lg[i] = ld_cg(row + e);
-    bs[i] = ld_ca(bias + e);
+    lg[i] = ORDERED ? ld_cg(row + e) : __ldg(row + e);
+    bs[i] = ORDERED ? ld_ca(bias + e) : __ldg(bias + e);
   }
   uint64_t cand[EPL];
   float sc[EPL];
