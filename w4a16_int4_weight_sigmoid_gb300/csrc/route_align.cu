@@ -44,26 +44,36 @@ __global__ void __launch_bounds__(kThreads) route_align_kernel(RouteIn r, AlignA
 }
 
 // The smallest batches (M * topk <= 32 assignments, e.g. one decode token at
-// top-8): one small CTA without the general align's per-warp tables.  Warp
-// t routes token t (ids kept in shared memory as well as written out); warp
-// 0 then holds assignment f in lane f: a stable rank per expert from
-// __match_any_sync, the present experts' order and offsets from a 32-entry
-// table; finally every thread fills counts and offsets for its experts by a
-// binary search in that table.  Outputs are those of the general kernels.
-constexpr int kTinyWarps = 4, kTinyMaxWarps = 8;
-template <int EPL>
-__global__ void __launch_bounds__(32 * kTinyMaxWarps) route_align_tiny_kernel(RouteIn r, AlignArgs a) {
+// top-8): one small CTA without the general align's per-warp tables.  Up to
+// kTinyCoopTokens tokens at topk <= kCoopMaxTopk, four warps route each token
+// together (EPW > 0: route_token_coop); otherwise warp t routes token t.  The
+// ids are kept in shared memory as well as written out; warp 0 then holds
+// assignment f in lane f: a stable rank per expert from __match_any_sync,
+// the present experts' order and offsets from a 32-entry table; finally
+// every thread fills counts and offsets for its experts by a binary search
+// in that table.  Outputs are those of the general kernels.
+constexpr int kTinyWarps = 4, kTinyMaxWarps = 8, kTinyCoopTokens = 4;
+template <int EPL, int EPW>
+__global__ void __launch_bounds__(32 * kCoopWarps * kTinyCoopTokens) route_align_tiny_kernel(RouteIn r, AlignArgs a) {
   __shared__ int s_id[32];                          // routed expert of assignment f
   __shared__ int s_le[32], s_pad[32];               // per lane of warp 0: expert it leads (or INT_MAX), pad
   __shared__ int t_e[32], t_end[32], t_cnt[32];     // present experts in id order
   __shared__ int s_nlead;
+  __shared__ CoopScratch s_coop[EPW > 0 ? kTinyCoopTokens : 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   grid_dep_wait();
   grid_dep_launch();
   zero_ints(r.zero, r.n_zero);
-  for (int t = warp; t < r.M; t += nw) {
-    const int id = route_token<EPL, true>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
-    if (lane < r.topk) s_id[t * r.topk + lane] = id;
+  if (EPW > 0) {   // blockDim = 32 kCoopWarps M: group g of four warps routes token g
+    const int g = warp / kCoopWarps, gw = warp % kCoopWarps;
+    const int id = route_token_coop<(EPW > 0 ? EPW : 1)>(r.logits, r.bias, g, r.E, r.topk, r.w, r.ids, s_coop[g],
+                                                      gw, 1 + g);
+    if (gw == 0 && lane < r.topk) s_id[g * r.topk + lane] = id;
+  } else {
+    for (int t = warp; t < r.M; t += nw) {
+      const int id = route_token<EPL, true>(r.logits, r.bias, t, r.E, r.topk, r.w, r.ids);
+      if (lane < r.topk) s_id[t * r.topk + lane] = id;
+    }
   }
   __syncthreads();
   const int n = a.n, bm = a.bm, E = a.E;
@@ -133,7 +143,11 @@ __global__ void __launch_bounds__(32 * kTinyMaxWarps) route_align_tiny_kernel(Ro
 template <int EPL>
 cudaError_t launch_tiny(const RouteIn& r, const AlignArgs& a, cudaStream_t st) {
   const int warps = r.M > kTinyWarps ? (r.M < kTinyMaxWarps ? r.M : kTinyMaxWarps) : kTinyWarps;
-  return launch_kernel(route_align_tiny_kernel<EPL>, dim3(1), dim3(32 * warps), 0, st, true, r, a);
+  return launch_kernel(route_align_tiny_kernel<EPL, 0>, dim3(1), dim3(32 * warps), 0, st, true, r, a);
+}
+template <int EPW>
+cudaError_t launch_tiny_coop(const RouteIn& r, const AlignArgs& a, cudaStream_t st) {
+  return launch_kernel(route_align_tiny_kernel<1, EPW>, dim3(1), dim3(32 * kCoopWarps * r.M), 0, st, true, r, a);
 }
 
 template <int EPL, int PER>
@@ -184,6 +198,14 @@ cudaError_t route_align_launch(const float* logits, const float* bias, int M, in
   a.ws_rank = nullptr;
   a.ws_counts = nullptr;
   const int epl = (E_total + 31) / 32;
+  if (a.n <= 32 && M >= 1 && M <= kTinyCoopTokens && topk <= kCoopMaxTopk) {
+    const int epw = (E_total + 32 * kCoopWarps - 1) / (32 * kCoopWarps);
+    if (epw <= 1) return launch_tiny_coop<1>(r, a, st);
+    if (epw <= 2) return launch_tiny_coop<2>(r, a, st);
+    if (epw <= 3) return launch_tiny_coop<3>(r, a, st);
+    if (epw <= 4) return launch_tiny_coop<4>(r, a, st);
+    return launch_tiny_coop<8>(r, a, st);
+  }
   if (a.n <= 32) {
     if (epl <= 1) return launch_tiny<1>(r, a, st);
     if (epl <= 2) return launch_tiny<2>(r, a, st);

@@ -1,5 +1,6 @@
-// Sigmoid + bias top-k routing of one token by one warp (device code shared
-// by the router kernel and the fused route+align kernel).
+// Sigmoid + bias top-k routing of one token by one warp, or by a group of
+// four warps (device code shared by the router kernel and the fused
+// route+align kernel).
 //
 // Buffers: [Router] "코드 분석" (arg_plan: logits, bias, topk_weights,
 // topk_ids).  The sigmoid is the fixed binary32 op sequence documented in
@@ -113,6 +114,94 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, con
     const size_t o = static_cast<size_t>(t) * topk + lane;
     id_out[o] = my_id;
     w_out[o] = __fdiv_rn(my_s, S);
+  }
+  return my_id;
+}
+
+// One token routed by a group of kCoopWarps warps (kCoopWarps * 32 threads):
+// warp gw of the group holds experts e = 32 gw + lane + 128 i (EPW per lane,
+// 128 EPW >= E), takes the top-k of its own experts by the same rounds as
+// route_token (any of the token's top-k is in its warp's top-k), and writes
+// them to shared memory; after a barrier the group's warp 0 ranks the
+// kCoopWarps * topk candidates by counting the larger keys (keys of real
+// experts are distinct; key 0 marks no candidate).  Same outputs, bit for
+// bit, as route_token; a quarter of the sigmoids and shorter maxima per
+// warp.  topk <= kCoopMaxTopk.  bar: named barrier of the group (128
+// threads).  Returns, in lanes 0 .. topk-1 of the group's warp 0, the id of
+// that rank (other warps: -1).  Ordered loads: the callers are programmatic
+// launches (see grid_dep_wait).
+constexpr int kCoopWarps = 4, kCoopMaxTopk = 8;
+struct CoopScratch {
+  unsigned long long key[kCoopWarps * kCoopMaxTopk];
+  float s[kCoopWarps * kCoopMaxTopk];
+  int id[kCoopMaxTopk];
+  float ws[kCoopMaxTopk];
+};
+template <int EPW>
+__device__ __forceinline__ int route_token_coop(const float* __restrict__ logits, const float* __restrict__ bias,
+                                                 int t, int E, int topk, float* __restrict__ w_out,
+                                                 int32_t* __restrict__ id_out, CoopScratch& cs, int gw, int bar) {
+  const int lane = threadIdx.x & 31;
+  const float* row = logits + static_cast<size_t>(t) * E;
+  float lg[EPW], bs[EPW];
+#pragma unroll
+  for (int i = 0; i < EPW; ++i) {
+    const int e = min(32 * gw + lane + 128 * i, E - 1);
+    lg[i] = ld_cg(row + e);
+    bs[i] = ld_ca(bias + e);
+  }
+  uint64_t cand[EPW];
+  float sc[EPW];
+#pragma unroll
+  for (int i = 0; i < EPW; ++i) {
+    const int e = 32 * gw + lane + 128 * i;
+    sc[i] = sigmoid_spec(lg[i]);
+    cand[i] = e < E ? pack_key(__fadd_rn(sc[i], bs[i]), e) : 0;
+  }
+  for (int r = 0; r < topk; ++r) {
+    uint64_t best = cand[0];
+#pragma unroll
+    for (int i = 1; i < EPW; ++i) best = cand[i] > best ? cand[i] : best;
+    const uint32_t hi = static_cast<uint32_t>(best >> 32);
+    const uint32_t top_hi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t top_lo =
+        __reduce_max_sync(0xffffffffu, hi == top_hi ? static_cast<uint32_t>(best) : 0u);
+    const int id = static_cast<int>(0xFFFFFFFFu - top_lo);
+    const int owner = id & 31, slot = id >> 7;   // e = 32 gw + owner + 128 slot
+    float s_mine = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPW; ++i) {
+      if (i == slot) {
+        s_mine = sc[i];
+        if (lane == owner) cand[i] = 0;
+      }
+    }
+    const float s_win = __shfl_sync(0xffffffffu, s_mine, owner);
+    if (lane == 0) {
+      cs.key[gw * topk + r] = (static_cast<uint64_t>(top_hi) << 32) | top_lo;
+      cs.s[gw * topk + r] = s_win;
+    }
+  }
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kCoopWarps * 32) : "memory");
+  if (gw != 0) return -1;
+  const int nc = kCoopWarps * topk;
+  const uint64_t mine = lane < nc ? cs.key[lane] : 0;
+  int rank = 0;
+  for (int m = 0; m < nc; ++m) rank += cs.key[m] > mine ? 1 : 0;
+  if (lane < nc && mine != 0 && rank < topk) {
+    cs.id[rank] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine));
+    cs.ws[rank] = cs.s[lane];
+  }
+  __syncwarp();
+  // S = s_0 + s_1 + ... in rank order, binary32
+  float S = cs.ws[0];
+  for (int r = 1; r < topk; ++r) S = __fadd_rn(S, cs.ws[r]);
+  int my_id = 0;
+  if (lane < topk) {
+    my_id = cs.id[lane];
+    const size_t o = static_cast<size_t>(t) * topk + lane;
+    id_out[o] = my_id;
+    w_out[o] = __fdiv_rn(cs.ws[lane], S);
   }
   return my_id;
 }
