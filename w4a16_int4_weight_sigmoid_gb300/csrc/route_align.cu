@@ -48,15 +48,17 @@ __global__ void __launch_bounds__(kThreads) route_align_kernel(RouteIn r, AlignA
 // kTinyCoopTokens tokens at topk <= kCoopMaxTopk, four warps route each token
 // together (EPW > 0: route_token_coop); otherwise warp t routes token t.  The
 // ids are kept in shared memory as well as written out; warp 0 then holds
-// assignment f in lane f: a stable rank per expert from __match_any_sync,
-// the present experts' order and offsets from a 32-entry table; finally
-// every thread fills counts and offsets for its experts by a binary search
-// in that table.  Outputs are those of the general kernels.
+// assignment f in lane f and ranks the assignments by ballots of the expert
+// ids' bits (no shared-memory table walk: __match_any_sync and a 32-step
+// loop took ~1400 cycles on GB300), writing the present experts' table; the
+// whole CTA then fills padding, block map, counts and offsets in one pass
+// over that table (a binary search per expert took ~2500 cycles).  Outputs
+// are those of the general kernels.
 constexpr int kTinyWarps = 4, kTinyMaxWarps = 8, kTinyCoopTokens = 4;
 template <int EPL, int EPW>
-__global__ void __launch_bounds__(32 * kCoopWarps * kTinyCoopTokens) route_align_tiny_kernel(RouteIn r, AlignArgs a) {
+__global__ void __launch_bounds__(EPW > 0 ? 32 * kCoopWarps * kTinyCoopTokens : 32 * kTinyMaxWarps)
+route_align_tiny_kernel(RouteIn r, AlignArgs a) {
   __shared__ int s_id[32];                          // routed expert of assignment f
-  __shared__ int s_le[32], s_pad[32];               // per lane of warp 0: expert it leads (or INT_MAX), pad
   __shared__ int t_e[32], t_end[32], t_cnt[32];     // present experts in id order
   __shared__ int s_nlead;
   __shared__ CoopScratch s_coop[EPW > 0 ? kTinyCoopTokens : 1];
@@ -78,65 +80,84 @@ __global__ void __launch_bounds__(32 * kCoopWarps * kTinyCoopTokens) route_align
   __syncthreads();
   const int n = a.n, bm = a.bm, E = a.E;
   if (warp == 0) {
+    // Assignment f in lane f.  From ballots of the expert id's bits, high to
+    // low (E <= 1024): eq = the lanes holding my expert, lt = the lanes
+    // holding a smaller one (stable rank = my place among eq).
     int e = lane < n ? s_id[lane] - a.begin : -1;
-    if (e < 0 || e >= E) e = -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    const int leader = __ffs(peers) - 1;
-    const bool lead = e >= 0 && lane == leader;
-    const int cnt = __popc(peers);
-    const int pad = lead ? (cnt + bm - 1) / bm * bm : 0;
-    s_le[lane] = lead ? e : 0x7fffffff;
-    s_pad[lane] = pad;
-    __syncwarp();
-    // order among the present experts and the padded rows below this one
-    int below = 0, off = 0;
-    if (lead) {
-#pragma unroll 8
-      for (int l = 0; l < 32; ++l) {
-        if (s_le[l] < e) {
-          ++below;
-          off += s_pad[l];
-        }
-      }
-      t_e[below] = e;
-      t_end[below] = off + pad;
-      t_cnt[below] = cnt;
-    }
-    const uint32_t leaders = __ballot_sync(0xffffffffu, lead);
-    int total = pad;
+    const bool valid = e >= 0 && e < E;
+    if (!valid) e = 0;
+    uint32_t lt = 0, eq = __ballot_sync(0xffffffffu, valid);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-    off = __shfl_sync(0xffffffffu, off, leader);
+    for (int b = 9; b >= 0; --b) {
+      const bool bit = (e >> b) & 1;
+      const uint32_t ones = __ballot_sync(0xffffffffu, valid && bit);
+      if (bit) {
+        lt |= eq & ~ones;
+        eq &= ones;
+      } else {
+        eq &= ~ones;
+      }
+    }
+    const int cnt = __popc(eq);
+    const bool lead = valid && lane == __ffs(eq) - 1;
+    const int nb = lead ? (cnt + bm - 1) / bm : 0;   // blocks of my expert (<= 4: n <= 32, bm >= 8)
+    const uint32_t leaders = __ballot_sync(0xffffffffu, lead);
+    // blocks of the experts below mine, and of all, summed from their bits
+    int below_blocks = 0, all_blocks = 0;
+#pragma unroll
+    for (int b = 0; b < 3; ++b) {
+      const uint32_t bits = __ballot_sync(0xffffffffu, (nb >> b) & 1);
+      below_blocks += __popc(bits & lt) << b;
+      all_blocks += __popc(bits) << b;
+    }
+    const int off = below_blocks * bm;
     if (lane < n) {
-      if (e >= 0) {
-        const int pos = off + rank;
+      if (valid) {
+        const int pos = off + __popc(eq & ((1u << lane) - 1u));
         a.sorted[pos] = lane;
         if (a.positions) a.positions[lane] = pos;
       } else if (a.positions) {
         a.positions[lane] = -1;
       }
     }
-    if (lead) {
-      for (int p = off + cnt; p < off + pad; ++p) a.sorted[p] = a.sentinel;
-      for (int b = off / bm; b < (off + pad) / bm; ++b) a.expert_ids[b] = e;
+    if (lead) {   // the present experts in id order
+      const int k = __popc(lt & leaders);
+      t_e[k] = e;
+      t_end[k] = off + nb * bm;
+      t_cnt[k] = cnt;
     }
     if (lane == 0) {
       s_nlead = __popc(leaders);
-      a.ntpp[0] = total;
+      a.ntpp[0] = all_blocks * bm;
     }
   }
   __syncthreads();
-  // every expert x: count, and the padded rows of the present experts below x
-  const int nlead = s_nlead;
-  for (int x = threadIdx.x; x <= E; x += blockDim.x) {
-    int lo = 0, hi = nlead;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (t_e[mid] < x) lo = mid + 1; else hi = mid;
+  // The whole CTA, one pass over the present experts: each one's padding
+  // rows and blocks (at most 127 and 4, blockDim >= 128), and for the
+  // thread's experts x the count and the padded rows below x.
+  const int nlead = s_nlead, bd = blockDim.x, tid = threadIdx.x;
+  constexpr int kMaxX = (1024 + 1 + 127) / 128;   // experts per thread at E <= 1024, blockDim >= 128
+  int xoff[kMaxX], xcnt[kMaxX];
+#pragma unroll
+  for (int j = 0; j < kMaxX; ++j) xoff[j] = xcnt[j] = 0;
+  int start = 0;
+  for (int k = 0; k < nlead; ++k) {
+    const int ek = t_e[k], endk = t_end[k], ck = t_cnt[k];
+#pragma unroll
+    for (int j = 0; j < kMaxX; ++j) {
+      const int x = tid + j * bd;
+      if (ek < x) xoff[j] = endk;
+      if (ek == x) xcnt[j] = ck;
     }
-    a.offsets[x] = lo == 0 ? 0 : t_end[lo - 1];
-    if (x < E) a.counts[x] = (lo < nlead && t_e[lo] == x) ? t_cnt[lo] : 0;
+    if (start + ck + tid < endk) a.sorted[start + ck + tid] = a.sentinel;
+    if (start / bm + tid < endk / bm) a.expert_ids[start / bm + tid] = ek;
+    start = endk;
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxX; ++j) {
+    const int x = tid + j * bd;
+    if (x <= E) a.offsets[x] = xoff[j];
+    if (x < E) a.counts[x] = xcnt[j];
   }
 }
 
