@@ -153,12 +153,13 @@ int chord_moe_align(const int32_t* topk_ids, int M, int topk, int expert_begin, 
  * chord_moe_route followed by chord_moe_align in one call, with their
  * arguments and bit-identical outputs ([Router] "코드 분석" and "커널 내부
  * 로직 변경": the fused router kernel also produces the align buffers and
- * re-initialises its counters at entry).  For M <= 16 tokens (or up to 32
- * assignments) it is one launch of one CTA (one warp routes each token, then
- * the stable counting sort; up to 32 assignments without the general sort's
- * per-warp tables), which saves a launch and a round trip through the
- * topk_ids buffer; larger calls run the two kernels, whose router grid
- * spreads the tokens over many CTAs.
+ * re-initialises its counters at entry).  Small calls are one launch of one
+ * CTA, which saves a launch and a round trip through the topk_ids buffer: at
+ * topk <= 8 up to 4 tokens (four warps route each token, then a ballot-based
+ * stable sort of the at most 32 assignments); at larger topk up to 16 tokens
+ * or 32 assignments (one warp routes each token, then the stable counting
+ * sort).  Larger calls run the two kernels, whose router grid spreads the
+ * tokens over many CTAs.
  *   logits, bias, E_total, topk, topk_weights, topk_ids   as chord_moe_route
  *   expert_begin .. sorted_positions, workspace, ws_bytes as chord_moe_align
  *                  (the workspace is needed only when M*topk > 4096)

@@ -192,21 +192,24 @@ def check_route_align(logits, bias, k, begin, E_local, bm):
 @pytest.mark.parametrize("M", wl.ROUTER_ALIGN_M)
 @pytest.mark.parametrize("bm", wl.ROUTER_ALIGN_BM)
 def test_route_align_fused_router_workload(M, bm):
-    """One launch up to 16 tokens (M = 1: one warp; M = 8: one CTA); larger M
-    takes the two-launch path."""
+    """At top-8, one launch up to 4 tokens (M = 1: four warps route the
+    token); M = 8 and larger take the two-launch path."""
     logits, bias = wl.router_inputs(M, wl.ROUTER_ALIGN_E, wl.ROUTER_ALIGN_SEED)
     check_route_align(logits, bias, wl.ROUTER_ALIGN_TOPK, 0, wl.ROUTER_ALIGN_E, bm)
 
 
 @pytest.mark.parametrize("M,E,k,begin,E_local,bm", [
-    (16, 384, 8, 96, 48, 16),        # the largest one-launch batch, shard in the middle
+    (16, 384, 8, 96, 48, 16),        # two launches at top-8 (one CTA per token), shard in the middle
     (17, 384, 8, 0, 48, 8),          # one token more: two launches
     (16, 1024, 32, 0, 1024, 128),    # widest router and shard in one launch
     (7, 1, 1, 0, 1, 128),
     (9, 1000, 17, 500, 500, 64),
     (0, 384, 8, 0, 48, 16),
-    # up to 32 assignments: one warp routes and aligns
-    (32, 384, 1, 0, 384, 16),       # 32 tokens at top-1
+    # up to 32 assignments: one CTA routes and aligns (four warps a token at top-k <= 8, up to 4 tokens)
+    (32, 384, 1, 0, 384, 16),       # 32 tokens at top-1: two launches
+    (1, 1024, 8, 0, 1024, 128),     # widest router, expert ids up to 1023 in the ballot ranking
+    (4, 1024, 8, 512, 512, 8),      # shard in the middle of 1024 experts
+    (3, 384, 1, 0, 384, 64),        # top-1, three tokens
     (4, 384, 8, 100, 48, 128),      # 32 assignments, shard in the middle, long padding
     (3, 64, 8, 0, 64, 8),
     (2, 1024, 16, 0, 1024, 16),     # widest router

@@ -193,7 +193,7 @@ def chord_moe_route_align(logits, bias, topk: int, expert_begin: int, E_local: i
                           topk_weights, topk_ids, sorted_token_ids, expert_ids, num_tokens_post_padded,
                           expert_counts, expert_offsets, sorted_positions=None, workspace=None,
                           stream=None):
-    """chord_moe_route then chord_moe_align in one call (one launch for M <= 16)."""
+    """chord_moe_route then chord_moe_align in one call (one launch for small M)."""
     M, E_total = logits.shape
     i32 = torch.int32
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0

@@ -288,7 +288,7 @@ int route_align_impl(const float* logits, const float* bias, int M, int E_total,
       (M > 0 && (!logits || !bias || !topk_weights || !topk_ids)))
     return fail(CHORD_ERR_INVALID_ARG, "null pointer");
   const long long n = static_cast<long long>(M) * topk;
-  if (!chord::route_align_fits(M, n, E_local)) {
+  if (!chord::route_align_fits(M, topk, n, E_local)) {
     // more than one chunk: the two separate launches
     cudaError_t er = chord::route_launch(logits, bias, M, E_total, topk, topk_weights, topk_ids,
                                          static_cast<cudaStream_t>(stream), zero, n_zero);

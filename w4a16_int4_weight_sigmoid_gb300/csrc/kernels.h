@@ -16,7 +16,7 @@ cudaError_t route_launch(const float* logits, const float* bias, int M, int E, i
 int align_num_chunks(long long n);
 size_t align_workspace_bytes(long long n, int E_local);
 // Fused router + one-chunk align (one CTA): only when route_align_fits().
-bool route_align_fits(int M, long long assignments, int E_local);
+bool route_align_fits(int M, int topk, long long assignments, int E_local);
 cudaError_t route_align_launch(const float* logits, const float* bias, int M, int E_total, int topk,
                                int begin, int E_local, int bm, float* w, int32_t* ids, int32_t* sorted,
                                int32_t* expert_ids, int32_t* ntpp, int32_t* counts, int32_t* offsets,

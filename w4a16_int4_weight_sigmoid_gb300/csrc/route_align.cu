@@ -189,18 +189,24 @@ cudaError_t launch_fused(const RouteIn& r, const AlignArgs& a, cudaStream_t st) 
 
 }  // namespace
 
-// One CTA routes one token per warp: beyond kWarps tokens a warp would route
-// several in turn and the separate router grid is faster.  Up to 32
-// assignments the one-warp kernel takes any number of tokens.
-bool route_align_fits(int M, long long assignments, int E_local) {
-  return (M <= kWarps || assignments <= 32) && assignments <= kChunk && E_local >= 1 && E_local <= 1024;
+// At top-k <= kCoopMaxTopk, one launch only up to kTinyCoopTokens tokens
+// (four warps route each token): beyond that the router grid, four warps a
+// token, and the align kernel are faster (M = 8, 384 experts: 5.96 against
+// 6.98 us for the one-CTA form).  Otherwise one CTA routes one token per
+// warp: beyond kWarps tokens a warp would route several in turn and the
+// separate router grid is faster; up to 32 assignments the one-warp kernel
+// takes any number of tokens.
+bool route_align_fits(int M, int topk, long long assignments, int E_local) {
+  if (assignments > kChunk || E_local < 1 || E_local > 1024) return false;
+  if (topk <= kCoopMaxTopk) return M <= kTinyCoopTokens;
+  return M <= kWarps || assignments <= 32;
 }
 
 cudaError_t route_align_launch(const float* logits, const float* bias, int M, int E_total, int topk,
                                int begin, int E_local, int bm, float* w, int32_t* ids, int32_t* sorted,
                                int32_t* expert_ids, int32_t* ntpp, int32_t* counts, int32_t* offsets,
                                int32_t* positions, cudaStream_t st, int* zero, int n_zero) {
-  if (!route_align_fits(M, static_cast<long long>(M) * topk, E_local)) return cudaErrorInvalidValue;
+  if (!route_align_fits(M, topk, static_cast<long long>(M) * topk, E_local)) return cudaErrorInvalidValue;
   RouteIn r{logits, bias, M, E_total, topk, w, ids, zero, n_zero};
   AlignArgs a;
   a.ids = ids;
