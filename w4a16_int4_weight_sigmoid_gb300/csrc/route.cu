@@ -1,5 +1,6 @@
-// Sigmoid + bias top-k router: one warp per token, shuffle-based selection
-// (the per-token code is in route_impl.cuh).
+// Sigmoid + bias top-k router: up to 512 tokens at top-k <= 8 a CTA of four
+// warps per token, otherwise one warp per token; selection by warp
+// reductions (the per-token code is in route_impl.cuh).
 #include <cfloat>
 
 #include "common.cuh"
@@ -12,7 +13,7 @@ namespace {
 // Up to this many tokens the router is a programmatic launch (its launch
 // overlaps the kernel before it; logits read with ordered loads after the
 // wait): M = 1 3.38 -> 3.19 us, M = 128 3.87 -> 3.41 us per chained call on
-// GB300.  Above it, a plain launch with __ldg loads streams the logits
+// GB300 (one warp per token).  Above it, a plain launch with __ldg loads streams the logits
 // faster (M = 4096: 10.4 us against 11.0 us with ordered loads).
 constexpr int kChainedMaxM = 512;
 
