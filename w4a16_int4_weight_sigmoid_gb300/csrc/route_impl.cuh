@@ -123,7 +123,8 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, con
 // 128 EPW >= E), takes the top-k of its own experts by the same rounds as
 // route_token (any of the token's top-k is in its warp's top-k), and writes
 // them to shared memory; after a barrier the group's warp 0 ranks the
-// kCoopWarps * topk candidates by counting the larger keys (keys of real
+// kCoopWarps * topk candidates, one per lane, by counting the larger keys
+// of the other lanes (keys of real
 // experts are distinct; key 0 marks no candidate).  Same outputs, bit for
 // bit, as route_token; a quarter of the sigmoids and shorter maxima per
 // warp.  topk <= kCoopMaxTopk.  bar: named barrier of the group (128
@@ -186,8 +187,12 @@ __device__ __forceinline__ int route_token_coop(const float* __restrict__ logits
   if (gw != 0) return -1;
   const int nc = kCoopWarps * topk;
   const uint64_t mine = lane < nc ? cs.key[lane] : 0;
-  int rank = 0;
-  for (int m = 0; m < nc; ++m) rank += cs.key[m] > mine ? 1 : 0;
+  int rank = 0;   // from registers: independent shuffles (a loop over shared memory took ~740 cycles)
+#pragma unroll
+  for (int m = 0; m < kCoopWarps * kCoopMaxTopk; ++m) {
+    const uint64_t other = __shfl_sync(0xffffffffu, mine, m);   // 0 past the candidates
+    rank += other > mine ? 1 : 0;
+  }
   if (lane < nc && mine != 0 && rank < topk) {
     cs.id[rank] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine));
     cs.ws[rank] = cs.s[lane];
