@@ -245,8 +245,11 @@ class Replica:
                                  dtype=torch.uint8, device=dev)
         self.align_launches = 1 if wsb == 0 else 2
         self.gemm_launches = 3 if self.large else 2     # + the row gather on the tcgen05 path
-        # chord_moe_layer routes and aligns in one launch when M <= 16 tokens fit one align chunk
-        fused = M <= 16 and M * k <= 4096 and E <= 1024
+        # chord_moe_layer routes and aligns in one launch for small batches (the
+        # library's rule: one align chunk, and up to 4 tokens at top-k <= 8,
+        # else up to 16 tokens or 32 assignments)
+        n = M * k
+        fused = n <= 4096 and E <= 1024 and (M <= 4 if k <= 8 else (M <= 16 or n <= 32))
         self.layer_launches = (1 if fused else 1 + self.align_launches) + self.gemm_launches + 1
 
     # the layer's steps, each one C-ABI call (the calls chord_moe_layer makes)

@@ -1,8 +1,8 @@
-// Fused router + align for small batches (up to 16 tokens): one CTA
-// routes every token (one warp per token, the router's own code), then,
-// after a block barrier that
-// makes its topk_ids writes visible to all its threads, runs the one-chunk
-// stable counting sort over them.  One launch instead of two: [Router]
+// Fused router + align for small batches (up to 4 tokens at top-k <= 8, up to
+// 16 above): one CTA routes every token (four warps a token, or one warp a
+// token above top-8, the router's own code), then, after a block barrier
+// that makes its topk_ids writes visible to all its threads, runs the
+// one-chunk stable sort over them.  One launch instead of two: [Router]
 // "코드 분석" and "커널 내부 로직 변경" fuse routing and align (with counters
 // re-initialised at entry) for the same reason -- at decode sizes both
 // kernels are launch- and latency-bound.  Outputs are bit-identical to
